@@ -1,0 +1,219 @@
+/*
+ * car.h -- C ABI of libcar: one-shot rank-sum reduce, fused residual add +
+ * RMSNorm, and LL / LL128 line encode, validate and decode-reduce, for one
+ * GB300 (sm_103a).
+ *
+ * The W "ranks" are W separate device buffers on the same GPU: they stand in
+ * for the peer-mapped buffers a multi-GPU one-shot all-reduce reads.  There is
+ * no cross-GPU barrier, no IPC and no transport; every entry point runs
+ * hand-written CUDA kernels on the caller's stream.
+ *
+ * Pages the operations come from (title, then section):
+ *   P1  "SGLang Custom AllReduce v1 线程模型和工作原理细节"
+ *   P2  "NCCL 专家课程 14：Simple、LL、LL128 的线格式、同步与真实性能边界"
+ *   P3  "0-custom-all-reduce" (SGLang JIT custom all-reduce notes)
+ *   P4  "用 Triton + Symmetric Memory 写一个 AllReduce + RMSNorm 融合算子"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Shapes.  A handle fixes W (number of rank buffers, 1..16), M rows, N
+ *   columns and the element type.  Every [M, N] tensor is row-major and
+ *   contiguous; D = M*N*s bytes per rank (s = 2 for bf16/fp16, 4 for fp32).
+ *   N*s must be a multiple of 16 so that each row starts on a 16-byte
+ *   boundary (P1 "线程模型：16 字节一个单位": the message is processed in
+ *   16-byte packed units; P3 "2. 线程怎么分活").
+ * - Pointers.  "dev" pointers are device memory on the handle's device,
+ *   owned by the caller, and must be 16-byte aligned.  Pointer tables
+ *   (inputs, wires) are host arrays of W device pointers, read during the
+ *   call only.  The library never frees caller memory.
+ * - Streams.  `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *   default stream.  Launches are asynchronous: a CAR_OK return means the work
+ *   was queued; results are valid once the stream has reached that point.
+ * - Errors.  Arguments are checked before anything is queued; a failed check
+ *   returns its code and launches nothing.  No entry point throws, traps,
+ *   spins without bound or calls exit.  CUDA errors seen at launch return
+ *   CAR_ERR_CUDA; car_last_error() gives the text.
+ * - Threads.  Distinct handles may be used from distinct threads.  One
+ *   handle must not be used by two threads at once.
+ */
+#ifndef CAR_H
+#define CAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CAR_BF16 = 0, CAR_FP16 = 1, CAR_FP32 = 2 } car_dtype;
+
+typedef enum {
+  CAR_OK = 0,
+  CAR_ERR_ARG = 1,        /* NULL pointer, W/M/N/dtype out of range, bad max_polls */
+  CAR_ERR_ALIGN = 2,      /* a device pointer not 16-byte aligned                   */
+  CAR_ERR_SIZE = 3,       /* N*s not a multiple of 16, size overflow, row too long  */
+  CAR_ERR_CUDA = 4,       /* CUDA runtime error (see car_last_error)                */
+  CAR_ERR_STALE_FLAG = 5, /* a decode found lines whose flag was not the expected one */
+  CAR_ERR_HANDLE = 6      /* NULL, destroyed or foreign handle                      */
+} car_status;
+
+typedef struct car_ctx car_ctx; /* opaque */
+
+/* Stale-line report of the last decode-reduce on a handle.  The caller sets
+ * `cap` and `entries` (a host array of cap (rank, line) pairs, may be NULL
+ * when cap == 0); the library fills n_stale (every stale (rank, line) pair
+ * found) and n_listed (pairs written, at most min(cap, CAR_STALE_LIST_MAX)).
+ * Order of the entries is unspecified; compare them as a set. */
+typedef struct {
+  uint64_t n_stale;
+  uint32_t n_listed;
+  uint32_t cap;
+  uint32_t (*entries)[2];
+} car_stale_report;
+
+/* Device-side capacity of the stale list kept per handle and per format. */
+#define CAR_STALE_LIST_MAX 65536u
+
+/* Longest row the fused kernel takes: N*s <= CAR_MAX_ROW_BYTES (64 KiB,
+ * e.g. N = 32768 bf16 or 16384 fp32). */
+#define CAR_MAX_ROW_BYTES (64u * 1024u)
+
+/* ---------------------------------------------------------------------- */
+/* Handles                                                                 */
+/* ---------------------------------------------------------------------- */
+
+/* Create a handle for W rank buffers of [M, N] elements of `dtype` on the
+ * current CUDA device.  The handle owns only its own small device scratch
+ * (stale-line counters and lists, about 1 MB) and the launch shapes it picks
+ * for this problem.  Errors: CAR_ERR_ARG (out == NULL, W not in 1..16, M < 1,
+ * N < 1, unknown dtype), CAR_ERR_SIZE (N*s % 16 != 0, or M*N*s overflows
+ * int64), CAR_ERR_CUDA (no device, allocation failed).  *out is set to NULL
+ * on error. */
+car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** out);
+
+/* Free the handle and its scratch.  Waits for nothing: the caller must make
+ * sure no queued work still uses it.  CAR_ERR_HANDLE for an unknown handle. */
+car_status car_destroy(car_ctx* h);
+
+/* ---------------------------------------------------------------------- */
+/* One-shot rank sum (P1 "1stage：kernel 全文与时间线", packed_reduce;     */
+/* P3 "3. 从所有 GPU 读" and "4. 求和(reduce_impl)")                       */
+/* ---------------------------------------------------------------------- */
+
+/* ar_out[i] = rne_T( (((f32(x_0[i]) + f32(x_1[i])) + ...) + f32(x_{W-1}[i])) )
+ * for every element i of the [M, N] problem: fp32 adds in rank order 0..W-1,
+ * seeded with rank 0's value, one round-to-nearest-even at the end (identity
+ * for fp32).  The order is fixed so that every caller gets the same bits.
+ *   inputs : host array of W dev pointers, each D bytes.
+ *   ar_out : dev, D bytes; may equal inputs[k] for one k (each element is read
+ *            before it is written, by the same thread).  Other overlap is
+ *            undefined.
+ * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG (NULL), CAR_ERR_ALIGN, CAR_ERR_CUDA. */
+car_status car_reduce(car_ctx* h, const void* const* inputs, void* ar_out, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Fused rank sum + residual add + RMSNorm                                 */
+/* (P4 "这个算子在算什么" and "总体设计")                                   */
+/* ---------------------------------------------------------------------- */
+
+/* Per row m and column j:
+ *   acc      = fp32 rank sum as in car_reduce (unrounded)
+ *   h        = acc + f32(residual[m,j])               (fp32 add)
+ *   residual_out[m,j] = rne_T(h);  ar_out[m,j] = rne_T(acc) when ar_out != NULL
+ *   rms      = rsqrt( (sum_j h^2) / N + eps )          (fp32, any order)
+ *   norm_out[m,j]     = rne_T( (h * rms) * f32(weight[j]) )
+ * ar and residual_out are bit-exact; norm_out depends on the order of the
+ * sum of squares and on rsqrtf, and lies within 2^-7*|ref| + 1e-5 of the
+ * exactly computed value.
+ *   inputs       : host array of W dev pointers, each [M, N].
+ *   residual     : dev [M, N].       weight : dev [N].
+ *   eps          : fp32 (e.g. 1e-6).
+ *   residual_out : dev [M, N]; may equal residual.
+ *   norm_out     : dev [M, N].
+ *   ar_out       : dev [M, N] or NULL; may equal inputs[k].
+ * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG (NULL, eps not finite or < 0),
+ * CAR_ERR_ALIGN, CAR_ERR_SIZE (N*s > CAR_MAX_ROW_BYTES), CAR_ERR_CUDA. */
+car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, const void* residual,
+                                       const void* weight, float eps, void* residual_out,
+                                       void* norm_out, void* ar_out, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* LL128 (P2 "LL128 的 128-byte line", "LL128 的 warp-level ready 检查")    */
+/* ---------------------------------------------------------------------- */
+
+/* Wire size of one rank's message: 128 * ceil(D / 120) bytes; 0 for an
+ * invalid handle. */
+size_t car_ll128_wire_bytes(car_ctx* h);
+
+/* Encode one rank's D data bytes into LL128 lines: line k holds data words
+ * 15k..15k+14 (uint64, little-endian, zero past the end of the data) in
+ * words 0..14 and `flag` in word 15.
+ *   data : dev, D bytes.   wire : dev, car_ll128_wire_bytes(h) bytes.
+ * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG, CAR_ERR_ALIGN, CAR_ERR_CUDA. */
+car_status car_ll128_encode(car_ctx* h, const void* data, uint64_t flag, void* wire, void* stream);
+
+/* Validate, decode and reduce W LL128 wires: line k of rank r is valid when
+ * its word 15 equals expected_flag.  A line found stale is checked again up
+ * to max_polls - 1 more times (re-reading the whole line each time); there
+ * is no unbounded wait.  For every line valid in all ranks, each element of
+ * its 120 data bytes is reduced as in car_reduce; the elements of a line
+ * stale in any rank are written as 0, and every stale (rank, line) pair is
+ * recorded for car_ll128_report.
+ *   wires   : host array of W dev pointers, each car_ll128_wire_bytes(h).
+ *   ar_out  : dev, D bytes.
+ *   max_polls : >= 1 (1 = check once).
+ * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG (NULL, max_polls < 1), CAR_ERR_ALIGN,
+ * CAR_ERR_CUDA.  Stale lines are reported by car_ll128_report, not here. */
+car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_t expected_flag,
+                                   int max_polls, void* ar_out, void* stream);
+
+/* Wait for the stream of the last car_ll128_decode_reduce on this handle and
+ * fill *out.  Returns CAR_ERR_STALE_FLAG when n_stale > 0, CAR_OK when none
+ * (or when no decode has run), CAR_ERR_HANDLE / CAR_ERR_ARG / CAR_ERR_CUDA. */
+car_status car_ll128_report(car_ctx* h, car_stale_report* out);
+
+/* ---------------------------------------------------------------------- */
+/* LL (P2 "LL 的 16-byte FIFO line", "LL 如何发布和等待 flag")              */
+/* ---------------------------------------------------------------------- */
+
+/* Wire size of one rank's message: 16 * ceil(D / 8) bytes; 0 for an invalid
+ * handle. */
+size_t car_ll_wire_bytes(car_ctx* h);
+
+/* Encode: line i = {low 32 bits of data word i, flag, high 32 bits, flag}.
+ *   data : dev, D bytes.   wire : dev, car_ll_wire_bytes(h) bytes. */
+car_status car_ll_encode(car_ctx* h, const void* data, uint32_t flag, void* wire, void* stream);
+
+/* Validate (both flags must equal expected_flag), decode (data1 +
+ * (data2 << 32)) and reduce W LL wires; same polling, zeroing and reporting
+ * rules as car_ll128_decode_reduce, with 8 data bytes per line. */
+car_status car_ll_decode_reduce(car_ctx* h, const void* const* wires, uint32_t expected_flag,
+                                int max_polls, void* ar_out, void* stream);
+
+/* Report of the last car_ll_decode_reduce, as car_ll128_report. */
+car_status car_ll_report(car_ctx* h, car_stale_report* out);
+
+/* ---------------------------------------------------------------------- */
+/* Diagnostics                                                              */
+/* ---------------------------------------------------------------------- */
+
+/* Static text for a status code. */
+const char* car_status_string(car_status s);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char* car_last_error(void);
+
+/* Override the fused kernel's launch shape for this handle (for tuning):
+ * cluster = CTAs per row (1, 2, 4 or 8), threads = threads per CTA (multiple
+ * of 32, at most 1024 for W <= 4 with vpt 1, else 512), vpt = 16-byte vectors
+ * per thread (1, or 2 when W is 1, 2, 4 or 8).  Passing 0 for all three
+ * restores the handle's automatic choice.  CAR_ERR_SIZE when
+ * cluster * threads * vpt does not cover a row; CAR_ERR_ARG for other values
+ * out of range. */
+car_status car_tune_fused(car_ctx* h, int cluster, int threads, int vpt);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CAR_H */

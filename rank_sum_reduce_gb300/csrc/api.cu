@@ -1,0 +1,397 @@
+// api.cu -- the C ABI of libcar (include/car.h): argument checks, handles,
+// launch shapes, stale-line reports.  Every operation runs in the kernels of
+// reduce.cu, fused.cu, ll128.cu and ll.cu; nothing here computes results.
+//
+// Argument rules follow the problem statement on the pages:
+//   P1 "SGLang Custom AllReduce v1 线程模型和工作原理细节", section
+//      "一次调用给 kernel 什么：参数与 grid" (message bytes a multiple of 16;
+//      same size and type on every rank) and "线程模型：16 字节一个单位"
+//      (16-byte aligned packed units);
+//   P3 "0-custom-all-reduce", "调用" (up to 16 ranks) and "5. 写回"
+//      (output may alias the input);
+//   P2 "NCCL 专家课程 14：Simple、LL、LL128 的线格式、同步与真实性能边界",
+//      "LL 如何发布和等待 flag" (waits are bounded: the page's loops check for
+//      abort; here a poll count bounds them).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "../../include/car.h"
+#include "car_device.cuh"
+#include "car_launch.h"
+
+static_assert(car::kStaleCap == CAR_STALE_LIST_MAX, "stale list capacity mismatch");
+
+struct car_ctx {
+  int W;
+  int64_t M, N;
+  int dtype;
+  int es;
+  int64_t D;            // bytes per rank
+  int64_t nvec;         // 16-byte vectors per rank
+  int vec_per_row;      // 16-byte vectors per row
+  int device;
+  int num_sms;
+  int reduce_grid;
+  bool fused_ok;        // row short enough for the fused kernel
+  car::FusedShape fused_auto;
+  car::FusedShape fused;
+  int64_t ll128_lines;
+  int ll128_encode_grid, ll128_decode_grid;
+  int64_t ll_lines;
+  int ll_encode_grid, ll_decode_grid;
+  car::StaleLog* log[2];       // [0] LL128, [1] LL (device)
+  cudaStream_t last_stream[2];
+  bool decoded[2];
+};
+
+namespace {
+
+std::mutex g_mu;
+std::unordered_set<const car_ctx*> g_live;
+thread_local char g_err[256] = "";
+
+car_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_err, sizeof(g_err), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return CAR_ERR_CUDA;
+}
+
+bool live(const car_ctx* h) {
+  if (!h) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_live.count(h) != 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every call on a handle: the handle is live and its device
+// is the current one.
+car_status check_handle(const car_ctx* h) {
+  if (!live(h)) return CAR_ERR_HANDLE;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device) {
+    snprintf(g_err, sizeof(g_err), "handle belongs to device %d, current device is %d", h->device, dev);
+    return CAR_ERR_ARG;
+  }
+  return CAR_OK;
+}
+
+car_status check_table(const car_ctx* h, const void* const* ptrs, car::RankPtrs* out) {
+  if (!ptrs) return CAR_ERR_ARG;
+  std::memset(out, 0, sizeof(*out));
+  for (int r = 0; r < h->W; r++) {
+    if (!ptrs[r]) return CAR_ERR_ARG;
+    if (!aligned16(ptrs[r])) return CAR_ERR_ALIGN;
+    out->p[r] = ptrs[r];
+  }
+  return CAR_OK;
+}
+
+car_status check_dev(const void* p) {
+  if (!p) return CAR_ERR_ARG;
+  return aligned16(p) ? CAR_OK : CAR_ERR_ALIGN;
+}
+
+int clamp_grid(int64_t needed, int per_sm, int num_sms) {
+  const int64_t cap = (int64_t)std::max(per_sm, 1) * num_sms;
+  return (int)std::max<int64_t>(1, std::min(needed, cap));
+}
+
+int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
+
+// Automatic shape of the fused kernel.
+//  * Many rows (M >= 2 x SMs): one CTA per row, the fewest vectors per
+//    thread that the compiled instances allow; split the row over a cluster
+//    only when a single CTA cannot cover it.
+//  * Few rows: split each row over up to 8 CTAs so that about one CTA per SM
+//    is busy, keeping at least 64 vectors per CTA.
+car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
+  car::FusedShape sh{1, 32, 1, 1};
+  if (M >= 2 * (int64_t)num_sms) {
+    for (int vpt = 1; vpt <= 2; vpt++) {
+      if (!car::fused_has_variant(W, vpt)) continue;
+      const int t = round_up32((V + vpt - 1) / vpt);
+      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{1, t, vpt, 1};
+    }
+  }
+  int c = 1;
+  if (M < 2 * (int64_t)num_sms) {
+    while (c < 8 && (int64_t)c * M < num_sms) c *= 2;
+    while (c > 1 && V / c < 64) c /= 2;
+  }
+  while (c < 8 && (V + c - 1) / c > car::fused_max_threads(W, 1)) c *= 2;
+  sh.cluster = c;
+  sh.vpt = 1;
+  sh.threads = std::max(32, round_up32((V + c - 1) / c));
+  return sh;
+}
+
+bool shape_valid(int W, int V, const car::FusedShape& sh) {
+  if (sh.cluster != 1 && sh.cluster != 2 && sh.cluster != 4 && sh.cluster != 8) return false;
+  if (!car::fused_has_variant(W, sh.vpt)) return false;
+  if (sh.threads < 32 || sh.threads % 32 != 0 || sh.threads > car::fused_max_threads(W, sh.vpt)) return false;
+  const int64_t chunk = (V + sh.cluster - 1) / sh.cluster;
+  return (int64_t)sh.threads * sh.vpt >= chunk;
+}
+
+car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
+  int groups = 0;
+  cudaError_t e = car::fused_resident_groups(h->dtype, h->W, sh, h->num_sms, &groups);
+  if (e != cudaSuccess) return cuda_fail(e, "fused occupancy");
+  sh.groups = (int)std::max<int64_t>(1, std::min<int64_t>(h->M, std::max(groups, 1)));
+  h->fused = sh;
+  return CAR_OK;
+}
+
+car_status decode_common(car_ctx* h, int which, const void* const* wires, int max_polls,
+                         void* ar_out, cudaStream_t s, car::RankPtrs* tbl) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if (max_polls < 1) return CAR_ERR_ARG;
+  if ((st = check_table(h, wires, tbl)) != CAR_OK) return st;
+  if ((st = check_dev(ar_out)) != CAR_OK) return st;
+  cudaError_t e = cudaMemsetAsync(&h->log[which]->n, 0, sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return cuda_fail(e, "reset stale count");
+  h->last_stream[which] = s;
+  h->decoded[which] = true;
+  return CAR_OK;
+}
+
+car_status report_common(car_ctx* h, int which, car_stale_report* out) {
+  if (!live(h)) return CAR_ERR_HANDLE;
+  if (!out || (out->cap > 0 && !out->entries)) return CAR_ERR_ARG;
+  out->n_stale = 0;
+  out->n_listed = 0;
+  if (!h->decoded[which]) return CAR_OK;
+  cudaError_t e = cudaStreamSynchronize(h->last_stream[which]);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned long long n = 0;
+  e = cudaMemcpy(&n, &h->log[which]->n, sizeof(n), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read stale count");
+  const uint64_t listed = std::min<uint64_t>(n, std::min<uint64_t>(out->cap, car::kStaleCap));
+  if (listed) {
+    e = cudaMemcpy(out->entries, h->log[which]->entry, listed * 2 * sizeof(uint32_t),
+                   cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read stale list");
+  }
+  out->n_stale = n;
+  out->n_listed = (uint32_t)listed;
+  return n ? CAR_ERR_STALE_FLAG : CAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* car_status_string(car_status s) {
+  switch (s) {
+    case CAR_OK: return "CAR_OK";
+    case CAR_ERR_ARG: return "CAR_ERR_ARG: invalid argument";
+    case CAR_ERR_ALIGN: return "CAR_ERR_ALIGN: device pointer not 16-byte aligned";
+    case CAR_ERR_SIZE: return "CAR_ERR_SIZE: unsupported size";
+    case CAR_ERR_CUDA: return "CAR_ERR_CUDA: CUDA runtime error";
+    case CAR_ERR_STALE_FLAG: return "CAR_ERR_STALE_FLAG: stale lines found";
+    case CAR_ERR_HANDLE: return "CAR_ERR_HANDLE: invalid handle";
+  }
+  return "unknown car_status";
+}
+
+const char* car_last_error(void) { return g_err; }
+
+car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** out) {
+  if (!out) return CAR_ERR_ARG;
+  *out = nullptr;
+  g_err[0] = 0;
+  if (W < 1 || W > car::kMaxRanks || M < 1 || N < 1) return CAR_ERR_ARG;
+  if (dtype != CAR_BF16 && dtype != CAR_FP16 && dtype != CAR_FP32) return CAR_ERR_ARG;
+  const int es = dtype == CAR_FP32 ? 4 : 2;
+  if (N > (int64_t)INT32_MAX / es || (N * es) % 16 != 0) return CAR_ERR_SIZE;
+  // whole message and both wire formats must stay far below int64 range
+  if (M > ((int64_t)1 << 56) / (N * es)) return CAR_ERR_SIZE;
+  const int64_t D = M * N * es;
+  if ((D + 119) / 120 > (int64_t)UINT32_MAX || D / 8 > (int64_t)UINT32_MAX) return CAR_ERR_SIZE;
+
+  car_ctx* h = new (std::nothrow) car_ctx();
+  if (!h) return CAR_ERR_ARG;
+  h->W = W;
+  h->M = M;
+  h->N = N;
+  h->dtype = (int)dtype;
+  h->es = es;
+  h->D = D;
+  h->nvec = D / 16;
+  h->vec_per_row = (int)(N * es / 16);
+  h->ll128_lines = (D + 119) / 120;
+  h->ll_lines = D / 8;
+
+  auto fail = [&](cudaError_t e, const char* where) {
+    for (auto*& p : h->log)
+      if (p) cudaFree(p);
+    delete h;
+    return cuda_fail(e, where);
+  };
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) return fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) return fail(e, "SM count");
+
+  int per_sm = 0, per_sm2 = 0;
+  if ((e = car::reduce_occupancy(h->dtype, W, &per_sm)) != cudaSuccess) return fail(e, "reduce occupancy");
+  const int64_t per_cta = (int64_t)car::kReduceThreads * car::reduce_vectors_per_thread(W);
+  h->reduce_grid = clamp_grid((h->nvec + per_cta - 1) / per_cta, per_sm, h->num_sms);
+
+  if ((e = car::ll128_occupancy(h->dtype, W, &per_sm, &per_sm2)) != cudaSuccess) return fail(e, "ll128 occupancy");
+  const int64_t pairs = (h->ll128_lines + 1) / 2;
+  const int64_t warps_needed = (pairs + 1) / 2;
+  const int64_t blocks_needed = (warps_needed + car::kWireThreads / 32 - 1) / (car::kWireThreads / 32);
+  h->ll128_decode_grid = clamp_grid(blocks_needed, per_sm, h->num_sms);
+  h->ll128_encode_grid = clamp_grid(blocks_needed, per_sm2, h->num_sms);
+
+  if ((e = car::ll_occupancy(h->dtype, W, &per_sm, &per_sm2)) != cudaSuccess) return fail(e, "ll occupancy");
+  h->ll_decode_grid = clamp_grid((h->ll_lines + car::kWireThreads - 1) / car::kWireThreads, per_sm, h->num_sms);
+  h->ll_encode_grid = clamp_grid((h->nvec + car::kWireThreads - 1) / car::kWireThreads, per_sm2, h->num_sms);
+
+  h->fused_ok = N * es <= (int64_t)CAR_MAX_ROW_BYTES;
+  if (h->fused_ok) {
+    h->fused_auto = auto_fused_shape(W, M, h->vec_per_row, h->num_sms);
+    car_status st = finish_fused_shape(h, h->fused_auto);
+    if (st != CAR_OK) {
+      delete h;
+      return st;
+    }
+    h->fused_auto = h->fused;
+  }
+
+  for (int k = 0; k < 2; k++) {
+    e = cudaMalloc(reinterpret_cast<void**>(&h->log[k]), sizeof(car::StaleLog));
+    if (e != cudaSuccess) return fail(e, "cudaMalloc stale log");
+    e = cudaMemset(h->log[k], 0, sizeof(unsigned long long) * 2);
+    if (e != cudaSuccess) return fail(e, "cudaMemset stale log");
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_live.insert(h);
+  }
+  *out = h;
+  return CAR_OK;
+}
+
+car_status car_destroy(car_ctx* h) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!h || g_live.erase(h) == 0) return CAR_ERR_HANDLE;
+  }
+  car_status st = CAR_OK;
+  for (auto* p : h->log) {
+    cudaError_t e = cudaFree(p);
+    if (e != cudaSuccess && st == CAR_OK) st = cuda_fail(e, "cudaFree");
+  }
+  delete h;
+  return st;
+}
+
+car_status car_tune_fused(car_ctx* h, int cluster, int threads, int vpt) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if (!h->fused_ok) return CAR_ERR_SIZE;
+  if (cluster == 0 && threads == 0 && vpt == 0) return finish_fused_shape(h, h->fused_auto);
+  car::FusedShape sh = h->fused_auto;
+  if (cluster) sh.cluster = cluster;
+  if (threads) sh.threads = threads;
+  if (vpt) sh.vpt = vpt;
+  if (sh.cluster != 1 && sh.cluster != 2 && sh.cluster != 4 && sh.cluster != 8) return CAR_ERR_ARG;
+  if (!car::fused_has_variant(h->W, sh.vpt)) return CAR_ERR_ARG;
+  if (sh.threads < 32 || sh.threads % 32 || sh.threads > car::fused_max_threads(h->W, sh.vpt)) return CAR_ERR_ARG;
+  if (!shape_valid(h->W, h->vec_per_row, sh)) return CAR_ERR_SIZE;
+  return finish_fused_shape(h, sh);
+}
+
+car_status car_reduce(car_ctx* h, const void* const* inputs, void* ar_out, void* stream) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  car::RankPtrs tbl;
+  if ((st = check_table(h, inputs, &tbl)) != CAR_OK) return st;
+  if ((st = check_dev(ar_out)) != CAR_OK) return st;
+  cudaError_t e = car::launch_reduce(h->dtype, h->W, tbl, ar_out, h->nvec, h->reduce_grid,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "rank_sum_reduce launch");
+}
+
+car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, const void* residual,
+                                       const void* weight, float eps, void* residual_out,
+                                       void* norm_out, void* ar_out, void* stream) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if (!std::isfinite(eps) || eps < 0.f) return CAR_ERR_ARG;
+  car::RankPtrs tbl;
+  if ((st = check_table(h, inputs, &tbl)) != CAR_OK) return st;
+  if ((st = check_dev(residual)) != CAR_OK) return st;
+  if ((st = check_dev(weight)) != CAR_OK) return st;
+  if ((st = check_dev(residual_out)) != CAR_OK) return st;
+  if ((st = check_dev(norm_out)) != CAR_OK) return st;
+  if (ar_out && !aligned16(ar_out)) return CAR_ERR_ALIGN;
+  if (!h->fused_ok) return CAR_ERR_SIZE;
+  cudaError_t e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out,
+                                    ar_out, h->M, h->N, h->vec_per_row, h->fused,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "reduce_residual_rmsnorm launch");
+}
+
+size_t car_ll128_wire_bytes(car_ctx* h) { return live(h) ? (size_t)(128 * h->ll128_lines) : 0; }
+size_t car_ll_wire_bytes(car_ctx* h) { return live(h) ? (size_t)(16 * h->ll_lines) : 0; }
+
+car_status car_ll128_encode(car_ctx* h, const void* data, uint64_t flag, void* wire, void* stream) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if ((st = check_dev(data)) != CAR_OK) return st;
+  if ((st = check_dev(wire)) != CAR_OK) return st;
+  cudaError_t e = car::launch_ll128_encode(data, h->D, h->ll128_lines, flag, wire, h->ll128_encode_grid,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll128_encode launch");
+}
+
+car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_t expected_flag,
+                                   int max_polls, void* ar_out, void* stream) {
+  car::RankPtrs tbl;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  car_status st = decode_common(h, 0, wires, max_polls, ar_out, s, &tbl);
+  if (st != CAR_OK) return st;
+  cudaError_t e = car::launch_ll128_decode_reduce(h->dtype, h->W, tbl, h->D, h->ll128_lines, expected_flag,
+                                                  max_polls, ar_out, h->log[0], h->ll128_decode_grid, s);
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll128_decode_reduce launch");
+}
+
+car_status car_ll128_report(car_ctx* h, car_stale_report* out) { return report_common(h, 0, out); }
+
+car_status car_ll_encode(car_ctx* h, const void* data, uint32_t flag, void* wire, void* stream) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if ((st = check_dev(data)) != CAR_OK) return st;
+  if ((st = check_dev(wire)) != CAR_OK) return st;
+  cudaError_t e = car::launch_ll_encode(data, h->D, flag, wire, h->ll_encode_grid,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll_encode launch");
+}
+
+car_status car_ll_decode_reduce(car_ctx* h, const void* const* wires, uint32_t expected_flag,
+                                int max_polls, void* ar_out, void* stream) {
+  car::RankPtrs tbl;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  car_status st = decode_common(h, 1, wires, max_polls, ar_out, s, &tbl);
+  if (st != CAR_OK) return st;
+  cudaError_t e = car::launch_ll_decode_reduce(h->dtype, h->W, tbl, h->D, expected_flag, max_polls,
+                                               ar_out, h->log[1], h->ll_decode_grid, s);
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll_decode_reduce launch");
+}
+
+car_status car_ll_report(car_ctx* h, car_stale_report* out) { return report_common(h, 1, out); }
+
+}  // extern "C"

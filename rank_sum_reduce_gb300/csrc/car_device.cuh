@@ -1,0 +1,176 @@
+// car_device.cuh -- device-side building blocks shared by libcar's kernels:
+// the rank pointer table, 16-byte loads, exact widening of packed bf16/fp16
+// to fp32, and the round-to-nearest-even narrowing (CUDA's cvt intrinsics).
+//
+// Pages (title, then section):
+//   P1 "SGLang Custom AllReduce v1 线程模型和工作原理细节"
+//   P3 "0-custom-all-reduce" (SGLang JIT custom all-reduce notes)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace car {
+
+constexpr int kMaxRanks = 16;  // P3 "调用": kMaxNumGPU raised to 16
+
+// W input pointers, passed by value in the kernel parameter block (128 B).
+// P1 "一次调用给 kernel 什么：参数与 grid" passes its table by pointer only so
+// that a captured graph can be back-filled; a single process has no such need.
+struct RankPtrs {
+  const void* p[kMaxRanks];
+};
+
+enum Dtype : int { kBF16 = 0, kFP16 = 1, kFP32 = 2 };
+
+// ---------------------------------------------------------------------------
+// 16-byte loads.  P1 "线程模型：16 字节一个单位": one thread moves 16 bytes
+// per instruction, the widest single global access.
+// ---------------------------------------------------------------------------
+
+// Read-only streaming load: rank inputs and the residual are read exactly once
+// per launch, so they bypass L1 allocation.  Safe with the documented aliasing
+// (output == one input): an address is read before the same thread writes it,
+// and never read again.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// Coherent (non read-only path) 16-byte load for wire lines, which a producer
+// may be writing while a bounded poll looks at them.
+__device__ __forceinline__ uint4 ld_wire(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Re-read for a poll: volatile, so every poll reaches the memory system.
+__device__ __forceinline__ uint4 ld_wire_poll(const void* p) {
+  uint4 v;
+  asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+__device__ __forceinline__ uint64_t lo64(uint4 v) { return (uint64_t)v.x | ((uint64_t)v.y << 32); }
+__device__ __forceinline__ uint64_t hi64(uint4 v) { return (uint64_t)v.z | ((uint64_t)v.w << 32); }
+__device__ __forceinline__ uint4 make16(uint64_t lo, uint64_t hi) {
+  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+// ---------------------------------------------------------------------------
+// Packed element types: a 16-byte vector holds 8 bf16/fp16 or 4 fp32 values.
+// Element 2k sits in the low half of 32-bit word k (little-endian layout).
+// Widening is exact; narrowing rounds to nearest, ties to even, with
+// subnormals kept (P1 "1stage：kernel 全文与时间线": upcast, accumulate in
+// fp32, one downcast; P3 "4. 求和": __float22bfloat162_rn).
+// ---------------------------------------------------------------------------
+template <int DT>
+struct Pack;
+
+template <>
+struct Pack<kBF16> {
+  static constexpr int kN = 8;
+  __device__ __forceinline__ static void widen(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(f[2 * i], f[2 * i + 1]));
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <>
+struct Pack<kFP16> {
+  static constexpr int kN = 8;
+  __device__ __forceinline__ static void widen(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const __half2 b = __float22half2_rn(make_float2(f[2 * i], f[2 * i + 1]));
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <>
+struct Pack<kFP32> {
+  static constexpr int kN = 4;
+  __device__ __forceinline__ static void widen(uint4 v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// acc = x_0; acc += x_r for r = 1..n-1, each an fp32 add rounded to nearest
+// (written with __fadd_rn so that no contraction or reassociation can occur).
+template <int DT, int W>
+__device__ __forceinline__ void rank_sum(const uint4 (&raw)[W], int n, float (&acc)[Pack<DT>::kN]) {
+  Pack<DT>::widen(raw[0], acc);
+#pragma unroll
+  for (int r = 1; r < W; r++) {
+    if (r < n) {
+      float t[Pack<DT>::kN];
+      Pack<DT>::widen(raw[r], t);
+#pragma unroll
+      for (int e = 0; e < Pack<DT>::kN; e++) acc[e] = __fadd_rn(acc[e], t[e]);
+    }
+  }
+}
+
+// Stale-line record of one decode: a count and the first kStaleCap pairs.
+constexpr uint32_t kStaleCap = 65536u;  // == CAR_STALE_LIST_MAX
+struct StaleLog {
+  unsigned long long n;
+  unsigned long long reserved;
+  uint32_t entry[kStaleCap][2];
+};
+
+__device__ __forceinline__ void log_stale(StaleLog* log, uint32_t rank, uint32_t line) {
+  const unsigned long long i = atomicAdd(&log->n, 1ull);
+  if (i < kStaleCap) {
+    log->entry[i][0] = rank;
+    log->entry[i][1] = line;
+  }
+}
+
+}  // namespace car

@@ -1,0 +1,57 @@
+// car_launch.h -- host-side launch entry points of libcar's kernels (internal).
+// Argument checking lives in api.cu; these functions only pick the template
+// instance for (dtype, W) and launch it on the given stream.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace car {
+
+struct RankPtrs;
+struct StaleLog;
+
+// ---- plain one-shot rank sum (reduce.cu) ----
+// nvec = number of 16-byte vectors per rank.  grid = CTAs of kReduceThreads.
+constexpr int kReduceThreads = 256;
+int reduce_vectors_per_thread(int W);
+cudaError_t reduce_occupancy(int dtype, int W, int* blocks_per_sm);
+cudaError_t launch_reduce(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
+                          cudaStream_t s);
+
+// ---- fused rank sum + residual + RMSNorm (fused.cu) ----
+struct FusedShape {
+  int cluster;  // CTAs per row (1, 2, 4, 8)
+  int threads;  // threads per CTA
+  int vpt;      // 16-byte vectors per thread (1, 2, 4)
+  int groups;   // row groups in the grid (grid = groups * cluster)
+};
+// Largest CTA the (W, vpt) instance is compiled for, and whether it exists
+// (vpt 2 exists for W in {1, 2, 4, 8}; vpt 1 for every W).
+int fused_max_threads(int W, int vpt);
+bool fused_has_variant(int W, int vpt);
+// How many row groups of this shape can be resident at once (0 on error).
+cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int num_sms, int* groups);
+cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
+                         const void* weight, float eps, void* residual_out, void* norm_out,
+                         void* ar_out, int64_t rows, int64_t cols, int vec_per_row,
+                         const FusedShape& sh, cudaStream_t s);
+
+// ---- LL128 (ll128.cu) ----
+constexpr int kWireThreads = 256;
+cudaError_t ll128_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm);
+cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
+                                void* wire, int grid, cudaStream_t s);
+cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
+                                       int64_t lines, uint64_t expected, int max_polls, void* out,
+                                       StaleLog* log, int grid, cudaStream_t s);
+
+// ---- LL (ll.cu) ----
+cudaError_t ll_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm);
+cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag, void* wire,
+                             int grid, cudaStream_t s);
+cudaError_t launch_ll_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
+                                    uint32_t expected, int max_polls, void* out, StaleLog* log,
+                                    int grid, cudaStream_t s);
+
+}  // namespace car

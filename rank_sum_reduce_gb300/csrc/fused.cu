@@ -1,0 +1,268 @@
+// fused.cu -- rank sum + residual add + RMSNorm in one pass over HBM.
+//
+// P4 "用 Triton + Symmetric Memory 写一个 AllReduce + RMSNorm 融合算子",
+// sections "这个算子在算什么" (ar = sum_r x_r; h = ar + residual;
+// rms = rsqrt(mean(h^2) + eps); out = (h * rms) * weight) and "总体设计"
+// (read every rank's row, fp32 sum, add residual and store residual_out, then
+// mean of squares, rsqrt, scale by weight and store norm_out, while the sum is
+// still in registers).  The rank sum itself follows P1
+// "1stage：kernel 全文与时间线" (fixed rank order, fp32, one rounding).
+//
+// GB300 design, differing from the page: the page gives a whole row to one
+// program and leaves the rest of the GPU idle at M = 1.  Here a row can be
+// split over a thread-block cluster of up to 8 CTAs on different SMs; each CTA
+// reduces its slice, and the partial sums of squares meet through distributed
+// shared memory behind one cluster barrier per row.  With many rows, one CTA
+// takes a row and CTAs loop over rows (grid capped at the resident count).
+// h never leaves registers.  Roofline: HBM, (W + 1 + outputs) * 16 bytes per
+// vector plus the weight row.
+#include <cooperative_groups.h>
+
+#include "car_device.cuh"
+#include "car_launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace car {
+namespace {
+
+struct FusedParams {
+  RankPtrs in;
+  const uint4* residual;
+  const uint4* weight;
+  uint4* residual_out;
+  uint4* norm_out;
+  uint4* ar_out;  // may be null
+  float eps;
+  float cols;     // N, exactly representable (N <= 2^24)
+  int64_t rows;
+  int vec_per_row;
+  int chunk;      // 16-byte vectors of a row handled by one CTA
+  int cluster;    // CTAs per row
+  int nranks;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+template <int W, int VPT>
+constexpr int max_threads() {
+  return (W > 0 && W <= 4 && VPT == 1) ? 1024 : 512;
+}
+
+template <int DT, int W, int VPT>
+__global__ void __launch_bounds__(max_threads<W, VPT>())
+    reduce_residual_rmsnorm_kernel(const FusedParams p) {
+  constexpr int E = Pack<DT>::kN;
+  constexpr int R = W > 0 ? W : kMaxRanks;
+  const int n = W > 0 ? W : p.nranks;
+  __shared__ float s_warp[32];
+  __shared__ float s_part[2];  // this CTA's partial, double-buffered by row parity
+  __shared__ float s_total;
+
+  const int C = p.cluster;
+  const int crank = C > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int64_t ngroups = gridDim.x / C;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int col0 = crank * p.chunk;
+  int parity = 0;
+
+  for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups) {
+    const int64_t rbase = row * (int64_t)p.vec_per_row;
+
+    // 1. all loads of this thread's vectors: W ranks + residual
+    uint4 raw[VPT][R];
+    uint4 res[VPT];
+    bool ok[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      const int v = threadIdx.x + k * blockDim.x;
+      ok[k] = v < p.chunk && col0 + v < p.vec_per_row;
+      if (ok[k]) {
+        const int64_t off = rbase + col0 + v;
+#pragma unroll
+        for (int r = 0; r < R; r++)
+          if (r < n) raw[k][r] = ld_stream(static_cast<const uint4*>(p.in.p[r]) + off);
+        res[k] = ld_stream(p.residual + off);
+      }
+    }
+
+    // 2. rank sum, residual add, first two outputs, sum of squares
+    float h[VPT][E];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      if (ok[k]) {
+        const int64_t off = rbase + col0 + threadIdx.x + k * blockDim.x;
+        float acc[E];
+        rank_sum<DT, R>(raw[k], n, acc);
+        if (p.ar_out) st16(p.ar_out + off, Pack<DT>::narrow(acc));
+        float rf[E];
+        Pack<DT>::widen(res[k], rf);
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+          h[k][e] = __fadd_rn(acc[e], rf[e]);
+          ss = fmaf(h[k][e], h[k][e], ss);
+        }
+        st16(p.residual_out + off, Pack<DT>::narrow(h[k]));
+      }
+    }
+
+    // 3. row statistic: warp shuffle, then shared memory across warps, then
+    //    (split rows) distributed shared memory across the cluster.  Every CTA
+    //    of a row adds the same partials in the same order, so all of them see
+    //    the same total.
+    ss = warp_sum(ss);
+    if (lane == 0) s_warp[warp] = ss;
+    __syncthreads();
+    if (warp == 0) {
+      float t = lane < nwarps ? s_warp[lane] : 0.f;
+      t = warp_sum(t);
+      if (lane == 0) {
+        if (C > 1) s_part[parity] = t;
+        else s_total = t;
+      }
+    }
+    if (C > 1) {
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+      if (warp == 0) {
+        float t = lane < C ? *cluster.map_shared_rank(&s_part[parity], lane) : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) s_total = t;
+      }
+      parity ^= 1;
+    }
+    __syncthreads();
+    const float rms = rsqrtf(__fdiv_rn(s_total, p.cols) + p.eps);
+
+    // 4. normalise and scale
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      if (ok[k]) {
+        const int col = col0 + threadIdx.x + k * blockDim.x;
+        float wf[E];
+        Pack<DT>::widen(__ldg(p.weight + col), wf);
+        float o[E];
+#pragma unroll
+        for (int e = 0; e < E; e++) o[e] = __fmul_rn(__fmul_rn(h[k][e], rms), wf[e]);
+        st16(p.norm_out + rbase + col, Pack<DT>::narrow(o));
+      }
+    }
+  }
+  // A CTA's partial may still be read by its peers: leave together.
+  if (C > 1) cg::this_cluster().sync();
+}
+
+using FusedFn = void (*)(const FusedParams);
+
+template <int DT>
+FusedFn pick_dt(int W, int vpt) {
+  if (vpt == 2) {
+    switch (W) {
+      case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 2>;
+      case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 2>;
+      case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 2>;
+      case 8: return reduce_residual_rmsnorm_kernel<DT, 8, 2>;
+      default: return nullptr;
+    }
+  }
+  if (vpt != 1) return nullptr;
+  switch (W) {
+    case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 1>;
+    case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 1>;
+    case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 1>;
+    case 8: return reduce_residual_rmsnorm_kernel<DT, 8, 1>;
+    case 16: return reduce_residual_rmsnorm_kernel<DT, 16, 1>;
+    default: return reduce_residual_rmsnorm_kernel<DT, 0, 1>;
+  }
+}
+
+FusedFn pick_fused(int dtype, int W, int vpt) {
+  switch (dtype) {
+    case kBF16: return pick_dt<kBF16>(W, vpt);
+    case kFP16: return pick_dt<kFP16>(W, vpt);
+    default: return pick_dt<kFP32>(W, vpt);
+  }
+}
+
+cudaLaunchConfig_t make_config(const FusedShape& sh, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sh.groups * sh.cluster), 1, 1);
+  cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)sh.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = sh.cluster > 1 ? 1 : 0;
+  return cfg;
+}
+
+}  // namespace
+
+int fused_max_threads(int W, int vpt) {
+  // W outside {1, 2, 4, 8, 16} runs the runtime-W instance, compiled for 512.
+  const bool compiled_w = W == 1 || W == 2 || W == 4;
+  return (vpt == 1 && compiled_w) ? 1024 : 512;
+}
+
+bool fused_has_variant(int W, int vpt) {
+  if (vpt == 1) return true;
+  return vpt == 2 && (W == 1 || W == 2 || W == 4 || W == 8);
+}
+
+cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int num_sms, int* groups) {
+  *groups = 0;
+  FusedFn fn = pick_fused(dtype, W, sh.vpt);
+  if (!fn) return cudaErrorInvalidValue;
+  if (sh.cluster == 1) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, reinterpret_cast<const void*>(fn), sh.threads, 0);
+    if (e != cudaSuccess) return e;
+    *groups = per_sm * num_sms;
+    return cudaSuccess;
+  }
+  cudaLaunchAttribute attr[1];
+  FusedShape probe = sh;
+  probe.groups = 1;
+  cudaLaunchConfig_t cfg = make_config(probe, 0, attr);
+  int clusters = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(fn), &cfg);
+  if (e != cudaSuccess) return e;
+  *groups = clusters;
+  return cudaSuccess;
+}
+
+cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
+                         const void* weight, float eps, void* residual_out, void* norm_out,
+                         void* ar_out, int64_t rows, int64_t cols, int vec_per_row,
+                         const FusedShape& sh, cudaStream_t s) {
+  FusedFn fn = pick_fused(dtype, W, sh.vpt);
+  if (!fn) return cudaErrorInvalidValue;
+  FusedParams p;
+  p.in = in;
+  p.residual = static_cast<const uint4*>(residual);
+  p.weight = static_cast<const uint4*>(weight);
+  p.residual_out = static_cast<uint4*>(residual_out);
+  p.norm_out = static_cast<uint4*>(norm_out);
+  p.ar_out = static_cast<uint4*>(ar_out);
+  p.eps = eps;
+  p.cols = (float)cols;
+  p.rows = rows;
+  p.vec_per_row = vec_per_row;
+  p.chunk = (vec_per_row + sh.cluster - 1) / sh.cluster;
+  p.cluster = sh.cluster;
+  p.nranks = W;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config(sh, s, attr);
+  return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace car

@@ -1,0 +1,123 @@
+// ll.cu -- LL line encode, and validate + decode + rank-sum reduce.
+//
+// P2 "NCCL 专家课程 14：Simple、LL、LL128 的线格式、同步与真实性能边界",
+// sections "LL 的 16-byte FIFO line" (a 16-byte line is {data1, flag1, data2,
+// flag2}, flags after their data) and "LL 如何发布和等待 flag" (the sender
+// writes the whole line in one 16-byte store; the receiver reads the line with
+// one 16-byte load, accepts it when both flags equal the expected flag, and
+// decodes data1 + (data2 << 32)).
+//
+// GB300 design: encode turns each 16-byte data vector into two lines (32
+// contiguous bytes per thread); decode gives one line per thread per rank, so
+// every access is a full 16-byte load and a warp stores 256 contiguous output
+// bytes.  Roofline: HBM, W * 16 wire bytes read + 8 bytes written per line.
+#include "car_device.cuh"
+#include "car_launch.h"
+
+namespace car {
+namespace {
+
+__global__ void __launch_bounds__(kWireThreads)
+    ll_encode_kernel(const uint4* __restrict__ data, const int64_t nvec, const uint32_t flag,
+                     uint4* __restrict__ wire) {
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += step) {
+    const uint4 d = ld_stream(data + i);
+    st16(wire + 2 * i, make_uint4(d.x, flag, d.y, flag));      // data word 2i
+    st16(wire + 2 * i + 1, make_uint4(d.z, flag, d.w, flag));  // data word 2i+1
+  }
+}
+
+template <int DT, int W>
+__global__ void __launch_bounds__(kWireThreads)
+    ll_decode_reduce_kernel(const RankPtrs wires, const int nranks, const int64_t lines,
+                            const uint32_t expected, const int max_polls, uint2* __restrict__ out,
+                            StaleLog* __restrict__ log) {
+  constexpr int R = W > 0 ? W : kMaxRanks;
+  const int n = W > 0 ? W : nranks;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += step) {
+    uint4 raw[R];
+#pragma unroll
+    for (int r = 0; r < R; r++)
+      if (r < n) raw[r] = ld_wire(static_cast<const uint4*>(wires.p[r]) + i);
+    uint32_t bad = 0;
+#pragma unroll
+    for (int r = 0; r < R; r++)
+      if (r < n && (raw[r].y != expected || raw[r].w != expected)) bad |= 1u << r;
+    for (int poll = 1; poll < max_polls && bad; poll++) {
+#pragma unroll
+      for (int r = 0; r < R; r++)
+        if (r < n) raw[r] = ld_wire_poll(static_cast<const uint4*>(wires.p[r]) + i);
+      bad = 0;
+#pragma unroll
+      for (int r = 0; r < R; r++)
+        if (r < n && (raw[r].y != expected || raw[r].w != expected)) bad |= 1u << r;
+    }
+    uint2 o = make_uint2(0u, 0u);
+    if (bad) {
+      for (int r = 0; r < n; r++)
+        if (bad >> r & 1u) log_stale(log, (uint32_t)r, (uint32_t)i);
+    } else {
+      // decoded data word of rank r: data1 | data2 << 32 = (raw.x, raw.z)
+      uint4 words[R];
+#pragma unroll
+      for (int r = 0; r < R; r++)
+        if (r < n) words[r] = make_uint4(raw[r].x, raw[r].z, 0u, 0u);
+      float acc[Pack<DT>::kN];
+      rank_sum<DT, R>(words, n, acc);
+      const uint4 s = Pack<DT>::narrow(acc);
+      o = make_uint2(s.x, s.y);
+    }
+    out[i] = o;
+  }
+}
+
+using DecodeFn = void (*)(const RankPtrs, const int, const int64_t, const uint32_t, const int,
+                          uint2*, StaleLog*);
+
+template <int DT>
+DecodeFn pick_dt(int W) {
+  switch (W) {
+    case 2: return ll_decode_reduce_kernel<DT, 2>;
+    case 4: return ll_decode_reduce_kernel<DT, 4>;
+    case 8: return ll_decode_reduce_kernel<DT, 8>;
+    case 16: return ll_decode_reduce_kernel<DT, 16>;
+    default: return ll_decode_reduce_kernel<DT, 0>;
+  }
+}
+
+DecodeFn pick_decode(int dtype, int W) {
+  switch (dtype) {
+    case kBF16: return pick_dt<kBF16>(W);
+    case kFP16: return pick_dt<kFP16>(W);
+    default: return pick_dt<kFP32>(W);
+  }
+}
+
+}  // namespace
+
+cudaError_t ll_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W)), kWireThreads, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      encode_blocks_per_sm, reinterpret_cast<const void*>(ll_encode_kernel), kWireThreads, 0);
+}
+
+cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag, void* wire,
+                             int grid, cudaStream_t s) {
+  ll_encode_kernel<<<grid, kWireThreads, 0, s>>>(static_cast<const uint4*>(data), data_bytes / 16,
+                                                 flag, static_cast<uint4*>(wire));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ll_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
+                                    uint32_t expected, int max_polls, void* out, StaleLog* log,
+                                    int grid, cudaStream_t s) {
+  pick_decode(dtype, W)<<<grid, kWireThreads, 0, s>>>(wires, W, data_bytes / 8, expected, max_polls,
+                                                      static_cast<uint2*>(out), log);
+  return cudaGetLastError();
+}
+
+}  // namespace car

