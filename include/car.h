@@ -173,6 +173,42 @@ car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_
  * (or when no decode has run), CAR_ERR_HANDLE / CAR_ERR_ARG / CAR_ERR_CUDA. */
 car_status car_ll128_report(car_ctx* h, car_stale_report* out);
 
+/* Allocation-free variant of car_ll128_decode_reduce.  The pages have no
+ * counterpart to it: it exists for callers that cannot call cudaMalloc and
+ * therefore cannot create a handle (car_create allocates the handle's
+ * stale-line log).  Examples: code running inside an allocator's own
+ * callbacks, processes whose caching pool already holds all free device
+ * memory, and latency-critical paths that cannot take the device-wide
+ * synchronisation an allocation or free can cause.
+ *
+ * It needs no handle and allocates nothing.  Its stale-line log is a fixed
+ * device array inside the library (CAR_STALE_LIST_MAX pairs, 512 KiB plus a
+ * 16-byte count) that every GPU which loads the library keeps until the
+ * process exits.  The first call on a device looks up that array's device
+ * address and the device's SM count, with the device current; make that
+ * first call before any stream capture on the device.
+ *
+ * Every call on a device shares the array and it keeps the last call's
+ * contents.  Each call clears the count on `stream` before its launch, so
+ * calls queued one after another on one stream are fine; calls that overlap
+ * on the GPU (two streams at once) race on the array and their reports are
+ * wrong.
+ *
+ * Arguments: the shape (W, M, N, dtype) and data as for car_create and
+ * car_ll128_decode_reduce (wires: W dev pointers of 128*ceil(M*N*s/120)
+ * bytes; ar_out: dev, M*N*s bytes).  stale_out: dev, 16-byte aligned,
+ * 16 + 8*cap bytes; after the call completes on `stream` it holds the
+ * uint64 count of stale (rank, line) pairs at byte 0, 8 reserved bytes, then
+ * min(count, cap) pairs of uint32 (rank, line) (bytes past those are
+ * leftovers).  cap may not exceed CAR_STALE_LIST_MAX.
+ * Errors: CAR_ERR_ARG (shape, NULL, max_polls < 1, device index > 63),
+ * CAR_ERR_SIZE (cap > CAR_STALE_LIST_MAX, with text in car_last_error(), or
+ * the shape rules of car_create), CAR_ERR_ALIGN, CAR_ERR_CUDA. */
+car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t N, car_dtype dtype,
+                                           const void* const* wires, uint64_t expected_flag,
+                                           int max_polls, void* ar_out, void* stale_out,
+                                           uint32_t cap, void* stream);
+
 /* ---------------------------------------------------------------------- */
 /* LL (P2 "LL 的 16-byte FIFO line", "LL 如何发布和等待 flag")              */
 /* ---------------------------------------------------------------------- */

@@ -57,6 +57,9 @@ _SIGS = {
     "car_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "car_last_error": (ctypes.c_char_p, []),
     "car_tune_fused": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "car_ll128_decode_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                       _pvp, ctypes.c_uint64, ctypes.c_int, _vp, _vp,
+                                                       ctypes.c_uint32, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -123,6 +126,14 @@ def _report(fn, h, cap: int):
 def car_ll128_report(h, cap: int = CAR_STALE_LIST_MAX):
     """Returns (status, n_stale, [(rank, line), ...])."""
     return _report(_lib.car_ll128_report, h, cap)
+
+
+def car_ll128_decode_reduce_noalloc(W: int, M: int, N: int, dtype: int, wires, expected_flag: int, max_polls: int,
+                                    ar_out: int, stale_out: int, cap: int, stream: int = 0) -> int:
+    """Handle-free LL128 decode-reduce that allocates nothing (see car.h):
+    stale_out is a device buffer of 16 + 8*cap bytes."""
+    return _lib.car_ll128_decode_reduce_noalloc(W, M, N, dtype, _table(wires) if wires is not None else None,
+                                                expected_flag, max_polls, ar_out, stale_out, cap, stream)
 
 
 def car_ll_wire_bytes(h) -> int:

@@ -189,6 +189,10 @@ car_status report_common(car_ctx* h, int which, car_stale_report* out) {
 
 }  // namespace
 
+namespace car {
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace car
+
 extern "C" {
 
 const char* car_status_string(car_status s) {

@@ -46,6 +46,9 @@ cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, 
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
                                        StaleLog* log, int grid, cudaStream_t s);
 
+// ---- diagnostics (api.cu): text returned by car_last_error() on this thread ----
+void set_last_error(const char* msg);
+
 // ---- LL (ll.cu) ----
 cudaError_t ll_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm);
 cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag, void* wire,
