@@ -55,8 +55,12 @@ typedef enum {
   CAR_ERR_SIZE = 3,       /* N*s not a multiple of 16, size overflow, row too long  */
   CAR_ERR_CUDA = 4,       /* CUDA runtime error (see car_last_error)                */
   CAR_ERR_STALE_FLAG = 5, /* a decode found lines whose flag was not the expected one */
-  CAR_ERR_HANDLE = 6      /* NULL, destroyed or foreign handle                      */
+  CAR_ERR_HANDLE = 6,     /* NULL, destroyed or foreign handle                      */
+  CAR_ERR_TIMEOUT = 7     /* a kernel gave up a bounded wait (see car_sync)         */
 } car_status;
+
+/* Kernels of car_reduce_residual_rmsnorm (see car_tune_fused). */
+typedef enum { CAR_FUSED_AUTO = 0, CAR_FUSED_ROWS = 1, CAR_FUSED_PIPELINE = 2 } car_fused_kernel;
 
 typedef struct car_ctx car_ctx; /* opaque */
 
@@ -240,14 +244,26 @@ const char* car_status_string(car_status s);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 const char* car_last_error(void);
 
-/* Override the fused kernel's launch shape for this handle (for tuning):
- * cluster = CTAs per row (1, 2, 4 or 8), threads = threads per CTA (multiple
- * of 32, at most 1024 for W <= 4 with vpt 1, else 512), vpt = 16-byte vectors
- * per thread (1, or 2 when W is 1, 2, 4 or 8).  Passing 0 for all three
- * restores the handle's automatic choice.  CAR_ERR_SIZE when
- * cluster * threads * vpt does not cover a row; CAR_ERR_ARG for other values
- * out of range. */
-car_status car_tune_fused(car_ctx* h, int cluster, int threads, int vpt);
+/* Choose the kernel of car_reduce_residual_rmsnorm for this handle (tuning
+ * and tests).  CAR_FUSED_ROWS: rows split over a cluster of cluster CTAs
+ * (1, 2, 4 or 8) of `threads` threads (multiple of 32, at most 1024 for
+ * W <= 4 with vpt 1, else 512), each thread holding vpt 16-byte vectors (1,
+ * or 2 when W is 1, 2, 4 or 8); 0 for a field keeps the automatic choice.
+ * CAR_FUSED_PIPELINE: one persistent CTA per SM streaming (row, rank) slices
+ * into a shared-memory ring with TMA bulk copies; cluster 0 or 1 gives each
+ * CTA whole rows, 2 splits every row over a CTA pair (needs an even number of
+ * 16-byte columns); threads and vpt must be 0; needs N*s <= 100 KiB per CTA.
+ * CAR_FUSED_AUTO (all fields 0) restores the automatic choice: the pipeline
+ * with whole rows when M >= 2 x the SM count, else rows.
+ * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_SIZE when the shape
+ * does not cover a row or the row does not fit the ring. */
+car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int vpt);
+
+/* Wait for `stream` and report whether any kernel of this handle gave up one
+ * of its bounded waits since the last car_sync (CAR_ERR_TIMEOUT; the flag is
+ * then cleared).  The pipelined fused kernel bounds every wait on its
+ * shared-memory barriers to about one second. */
+car_status car_sync(car_ctx* h, void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,13 +18,16 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcar.so")
 
 CAR_BF16, CAR_FP16, CAR_FP32 = 0, 1, 2
-CAR_OK, CAR_ERR_ARG, CAR_ERR_ALIGN, CAR_ERR_SIZE, CAR_ERR_CUDA, CAR_ERR_STALE_FLAG, CAR_ERR_HANDLE = range(7)
+CAR_OK, CAR_ERR_ARG, CAR_ERR_ALIGN, CAR_ERR_SIZE, CAR_ERR_CUDA, CAR_ERR_STALE_FLAG, CAR_ERR_HANDLE, CAR_ERR_TIMEOUT = \
+    range(8)
+CAR_FUSED_AUTO, CAR_FUSED_ROWS, CAR_FUSED_PIPELINE = 0, 1, 2
 CAR_STALE_LIST_MAX = 65536
 CAR_MAX_ROW_BYTES = 64 * 1024
 DTYPE_CODE = {"bf16": CAR_BF16, "fp16": CAR_FP16, "fp32": CAR_FP32}
 STATUS_NAME = {CAR_OK: "CAR_OK", CAR_ERR_ARG: "CAR_ERR_ARG", CAR_ERR_ALIGN: "CAR_ERR_ALIGN",
                CAR_ERR_SIZE: "CAR_ERR_SIZE", CAR_ERR_CUDA: "CAR_ERR_CUDA",
-               CAR_ERR_STALE_FLAG: "CAR_ERR_STALE_FLAG", CAR_ERR_HANDLE: "CAR_ERR_HANDLE"}
+               CAR_ERR_STALE_FLAG: "CAR_ERR_STALE_FLAG", CAR_ERR_HANDLE: "CAR_ERR_HANDLE",
+               CAR_ERR_TIMEOUT: "CAR_ERR_TIMEOUT"}
 
 
 class car_stale_report(ctypes.Structure):
@@ -56,7 +59,8 @@ _SIGS = {
     "car_ll_report": (ctypes.c_int, [_vp, ctypes.POINTER(car_stale_report)]),
     "car_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "car_last_error": (ctypes.c_char_p, []),
-    "car_tune_fused": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "car_tune_fused": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "car_sync": (ctypes.c_int, [_vp, _vp]),
     "car_ll128_decode_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                                        _pvp, ctypes.c_uint64, ctypes.c_int, _vp, _vp,
                                                        ctypes.c_uint32, _vp]),
@@ -161,8 +165,12 @@ def car_last_error() -> str:
     return _lib.car_last_error().decode()
 
 
-def car_tune_fused(h, cluster: int, threads: int, vpt: int) -> int:
-    return _lib.car_tune_fused(h, cluster, threads, vpt)
+def car_tune_fused(h, kernel: int, cluster: int, threads: int, vpt: int) -> int:
+    return _lib.car_tune_fused(h, kernel, cluster, threads, vpt)
+
+
+def car_sync(h, stream: int = 0) -> int:
+    return _lib.car_sync(h, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -256,5 +264,8 @@ class Car:
             check(st, "car_ll_report")
         return n, pairs
 
-    def tune_fused(self, cluster=0, threads=0, vpt=0):
-        check(car_tune_fused(self.h, cluster, threads, vpt), "car_tune_fused")
+    def tune_fused(self, kernel=CAR_FUSED_AUTO, cluster=0, threads=0, vpt=0):
+        check(car_tune_fused(self.h, kernel, cluster, threads, vpt), "car_tune_fused")
+
+    def sync(self, stream=None):
+        check(car_sync(self.h, _stream(stream)), "car_sync")

@@ -42,6 +42,12 @@ struct car_ctx {
   bool fused_ok;        // row short enough for the fused kernel
   car::FusedShape fused_auto;
   car::FusedShape fused;
+  bool tma_ok;          // row fits the shared-memory ring of the pipelined kernel
+  car::FusedTmaShape tma_auto;
+  car::FusedTmaShape tma;
+  int fused_kernel_auto;  // CAR_FUSED_ROWS or CAR_FUSED_PIPELINE
+  int fused_kernel;
+  unsigned int* d_err;  // bounded-wait failures reported by kernels (device)
   int64_t ll128_lines;
   int ll128_encode_grid, ll128_decode_grid;
   int64_t ll_lines;
@@ -142,6 +148,13 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
   return (int64_t)sh.threads * sh.vpt >= chunk;
 }
 
+// The pipelined kernel is as fast or faster once every SM streams at least two
+// rows (measured on GB300 at W=8, N=8192 bf16 and W=4, N=4096 fp32); below
+// that the row-split kernel keeps more SMs busy.
+int auto_fused_kernel(const car_ctx* h) {
+  return (h->tma_ok && h->M >= 2 * (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
+}
+
 car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
   int groups = 0;
   cudaError_t e = car::fused_resident_groups(h->dtype, h->W, sh, h->num_sms, &groups);
@@ -204,6 +217,7 @@ const char* car_status_string(car_status s) {
     case CAR_ERR_CUDA: return "CAR_ERR_CUDA: CUDA runtime error";
     case CAR_ERR_STALE_FLAG: return "CAR_ERR_STALE_FLAG: stale lines found";
     case CAR_ERR_HANDLE: return "CAR_ERR_HANDLE: invalid handle";
+    case CAR_ERR_TIMEOUT: return "CAR_ERR_TIMEOUT: a kernel gave up a bounded wait";
   }
   return "unknown car_status";
 }
@@ -239,6 +253,7 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   auto fail = [&](cudaError_t e, const char* where) {
     for (auto*& p : h->log)
       if (p) cudaFree(p);
+    if (h->d_err) cudaFree(h->d_err);
     delete h;
     return cuda_fail(e, where);
   };
@@ -264,6 +279,14 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   h->ll_encode_grid = clamp_grid((h->nvec + car::kWireThreads - 1) / car::kWireThreads, per_sm2, h->num_sms);
 
   h->fused_ok = N * es <= (int64_t)CAR_MAX_ROW_BYTES;
+  // The pipelined kernel takes whole rows by default: splitting rows over CTA
+  // pairs puts a cross-SM exchange on every row's critical path, which
+  // measured slower on GB300 than the quantisation it removes.
+  h->tma_ok = h->fused_ok && car::fused_tma_shape(M, h->vec_per_row, h->num_sms, 1, &h->tma);
+  h->tma_auto = h->tma;
+  if (h->tma_ok && (e = car::fused_tma_prepare(h->dtype, W, h->tma)) != cudaSuccess) return fail(e, "pipeline smem");
+  h->fused_kernel_auto = auto_fused_kernel(h);
+  h->fused_kernel = h->fused_kernel_auto;
   if (h->fused_ok) {
     h->fused_auto = auto_fused_shape(W, M, h->vec_per_row, h->num_sms);
     car_status st = finish_fused_shape(h, h->fused_auto);
@@ -274,6 +297,10 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
     h->fused_auto = h->fused;
   }
 
+  e = cudaMalloc(reinterpret_cast<void**>(&h->d_err), 16);
+  if (e != cudaSuccess) return fail(e, "cudaMalloc error word");
+  e = cudaMemset(h->d_err, 0, 16);
+  if (e != cudaSuccess) return fail(e, "cudaMemset error word");
   for (int k = 0; k < 2; k++) {
     e = cudaMalloc(reinterpret_cast<void**>(&h->log[k]), sizeof(car::StaleLog));
     if (e != cudaSuccess) return fail(e, "cudaMalloc stale log");
@@ -298,15 +325,34 @@ car_status car_destroy(car_ctx* h) {
     cudaError_t e = cudaFree(p);
     if (e != cudaSuccess && st == CAR_OK) st = cuda_fail(e, "cudaFree");
   }
+  cudaError_t e = cudaFree(h->d_err);
+  if (e != cudaSuccess && st == CAR_OK) st = cuda_fail(e, "cudaFree");
   delete h;
   return st;
 }
 
-car_status car_tune_fused(car_ctx* h, int cluster, int threads, int vpt) {
+car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int vpt) {
   car_status st = check_handle(h);
   if (st != CAR_OK) return st;
   if (!h->fused_ok) return CAR_ERR_SIZE;
-  if (cluster == 0 && threads == 0 && vpt == 0) return finish_fused_shape(h, h->fused_auto);
+  if (kernel == CAR_FUSED_AUTO) {
+    if (cluster || threads || vpt) return CAR_ERR_ARG;
+    h->fused_kernel = h->fused_kernel_auto;
+    h->tma = h->tma_auto;
+    return finish_fused_shape(h, h->fused_auto);
+  }
+  if (kernel == CAR_FUSED_PIPELINE) {
+    if (threads || vpt || (cluster != 0 && cluster != 1 && cluster != 2)) return CAR_ERR_ARG;
+    if (!h->tma_ok) return CAR_ERR_SIZE;
+    car::FusedTmaShape t;
+    if (!car::fused_tma_shape(h->M, h->vec_per_row, h->num_sms, cluster ? cluster : 1, &t)) return CAR_ERR_SIZE;
+    cudaError_t e = car::fused_tma_prepare(h->dtype, h->W, t);
+    if (e != cudaSuccess) return cuda_fail(e, "pipeline smem");
+    h->tma = t;
+    h->fused_kernel = CAR_FUSED_PIPELINE;
+    return CAR_OK;
+  }
+  if (kernel != CAR_FUSED_ROWS) return CAR_ERR_ARG;
   car::FusedShape sh = h->fused_auto;
   if (cluster) sh.cluster = cluster;
   if (threads) sh.threads = threads;
@@ -315,7 +361,23 @@ car_status car_tune_fused(car_ctx* h, int cluster, int threads, int vpt) {
   if (!car::fused_has_variant(h->W, sh.vpt)) return CAR_ERR_ARG;
   if (sh.threads < 32 || sh.threads % 32 || sh.threads > car::fused_max_threads(h->W, sh.vpt)) return CAR_ERR_ARG;
   if (!shape_valid(h->W, h->vec_per_row, sh)) return CAR_ERR_SIZE;
-  return finish_fused_shape(h, sh);
+  st = finish_fused_shape(h, sh);
+  if (st == CAR_OK) h->fused_kernel = CAR_FUSED_ROWS;
+  return st;
+}
+
+car_status car_sync(car_ctx* h, void* stream) {
+  if (!live(h)) return CAR_ERR_HANDLE;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int err = 0;
+  e = cudaMemcpy(&err, h->d_err, sizeof(err), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (!err) return CAR_OK;
+  e = cudaMemset(h->d_err, 0, sizeof(err));
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  snprintf(g_err, sizeof(g_err), "a kernel gave up a bounded wait (code %u)", err);
+  return CAR_ERR_TIMEOUT;
 }
 
 car_status car_reduce(car_ctx* h, const void* const* inputs, void* ar_out, void* stream) {
@@ -343,9 +405,13 @@ car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, co
   if ((st = check_dev(norm_out)) != CAR_OK) return st;
   if (ar_out && !aligned16(ar_out)) return CAR_ERR_ALIGN;
   if (!h->fused_ok) return CAR_ERR_SIZE;
-  cudaError_t e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out,
-                                    ar_out, h->M, h->N, h->vec_per_row, h->fused,
-                                    static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (h->fused_kernel == CAR_FUSED_PIPELINE)
+    e = car::launch_fused_tma(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out,
+                              h->d_err, h->M, h->N, h->vec_per_row, h->tma, static_cast<cudaStream_t>(stream));
+  else
+    e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out, h->M,
+                          h->N, h->vec_per_row, h->fused, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "reduce_residual_rmsnorm launch");
 }
 

@@ -37,6 +37,24 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
                          void* ar_out, int64_t rows, int64_t cols, int vec_per_row,
                          const FusedShape& sh, cudaStream_t s);
 
+// ---- fused, many rows: TMA bulk copies into a shared-memory ring (fused_tma.cu) ----
+struct FusedTmaShape {
+  int cluster;    // CTAs sharing each row (1 or 2)
+  int consumers;  // consumer threads (the CTA adds one producer warp)
+  int vpt;        // 16-byte vectors per consumer thread (1, 2, 4, 8)
+  int slots;      // ring depth in row slices
+  int grid;       // persistent CTAs
+  int smem;       // dynamic shared memory bytes
+};
+// False when the row does not fit the ring design.
+bool fused_tma_shape(int64_t rows, int vec_per_row, int num_sms, int cluster, FusedTmaShape* out);
+// Once per shape: allow the kernel instance its dynamic shared memory.
+cudaError_t fused_tma_prepare(int dtype, int W, const FusedTmaShape& sh);
+cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* residual, const void* weight,
+                             float eps, void* residual_out, void* norm_out, void* ar_out, unsigned int* err,
+                             int64_t rows, int64_t cols, int vec_per_row, const FusedTmaShape& sh,
+                             cudaStream_t s);
+
 // ---- LL128 (ll128.cu) ----
 constexpr int kWireThreads = 256;
 cudaError_t ll128_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm);

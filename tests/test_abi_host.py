@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(car):
 
 
 def test_status_strings(car):
-    for st in range(7):
+    for st in range(8):
         assert car.car_status_string(st).startswith(car.STATUS_NAME[st])
     assert "unknown" in car.car_status_string(99)
 
@@ -76,7 +76,8 @@ def test_calls_on_bad_handles(car):
     assert car.car_ll_decode_reduce(bogus, [16], 7, 1, 16) == car.CAR_ERR_HANDLE
     assert car.car_ll128_report(bogus)[0] == car.CAR_ERR_HANDLE
     assert car.car_ll_report(bogus)[0] == car.CAR_ERR_HANDLE
-    assert car.car_tune_fused(bogus, 1, 32, 1) == car.CAR_ERR_HANDLE
+    assert car.car_tune_fused(bogus, car.CAR_FUSED_ROWS, 1, 32, 1) == car.CAR_ERR_HANDLE
+    assert car.car_sync(bogus) == car.CAR_ERR_HANDLE
     assert car.car_ll128_wire_bytes(bogus) == 0 and car.car_ll_wire_bytes(bogus) == 0
 
 

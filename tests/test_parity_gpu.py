@@ -18,6 +18,10 @@ pytestmark = pytest.mark.gpu
 TOL_REL, TOL_ABS = 2.0**-7, 1e-5
 
 
+def car_elem(dtype):
+    return 4 if dtype == "fp32" else 2
+
+
 @pytest.fixture(scope="module")
 def car():
     if not torch.cuda.is_available():
@@ -144,14 +148,18 @@ def _fused_inputs(W, M, N, dtype, seed):
     return wl, xs, res, w
 
 
+@pytest.mark.parametrize("kernel", ["auto", "rows", "pipeline"])
 @pytest.mark.parametrize("W,M,N,dtype", FUSED_CASES)
-def test_fused_parity(car, W, M, N, dtype):
+def test_fused_parity(car, W, M, N, dtype, kernel):
     wl, xs, res, w = _fused_inputs(W, M, N, dtype, seed=2000 + W + M)
     dx = [x.to(DEV) for x in xs]
     dres, dw = res.to(DEV), w.to(DEV)
     ro, no, ar = torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)
     with car.Car(W, M, N, dtype) as c:
+        if kernel != "auto":
+            c.tune_fused(car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE)
         c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+        c.sync()
     torch.cuda.synchronize()
     ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, dtype)
     assert_bits_equal(ar, ref_ar, "ar")
@@ -175,9 +183,9 @@ def test_fused_every_launch_shape(car, cluster, threads, vpt):
         with car.Car(W, M, N, "bf16") as c:
             V = N * 2 // 16
             if cluster * threads * vpt < V:
-                assert car.car_tune_fused(c.h, cluster, threads, vpt) == car.CAR_ERR_SIZE
+                assert car.car_tune_fused(c.h, car.CAR_FUSED_ROWS, cluster, threads, vpt) == car.CAR_ERR_SIZE
                 continue
-            c.tune_fused(cluster, threads, vpt)
+            c.tune_fused(car.CAR_FUSED_ROWS, cluster, threads, vpt)
             c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
         torch.cuda.synchronize()
         rows = slice(None) if M <= 8 else torch.tensor([0, 1, M // 2, M - 2, M - 1])
@@ -186,6 +194,38 @@ def test_fused_every_launch_shape(car, cluster, threads, vpt):
         assert_bits_equal(ar[rows], ref_ar, "ar")
         assert_bits_equal(ro[rows], ref_ro, "residual_out")
         assert_norm_close(no[rows], ref_no)
+
+
+PIPELINE_CASES = [
+    # rows spread over every SM several times, partial last pass, every dtype, odd and large W
+    (8, 700, 8192, "bf16"), (4, 333, 4096, "fp32"), (3, 401, 1544, "fp16"), (16, 160, 2048, "bf16"),
+    (1, 155, 520, "bf16"), (5, 300, 16384, "bf16"), (2, 152, 8, "bf16"), (8, 2000, 1024, "bf16"),
+]
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
+@pytest.mark.parametrize("W,M,N,dtype", PIPELINE_CASES)
+def test_fused_pipeline_many_rows(car, W, M, N, dtype, cluster):
+    wl, xs, res, w = _fused_inputs(W, M, N, dtype, seed=5000 + W + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    ro, no, ar = torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)
+    with car.Car(W, M, N, dtype) as c:
+        V = N * car_elem(dtype) // 16
+        if cluster == 2 and V % 2:
+            assert car.car_tune_fused(c.h, car.CAR_FUSED_PIPELINE, 2, 0, 0) == car.CAR_ERR_SIZE
+            return
+        c.tune_fused(car.CAR_FUSED_PIPELINE, cluster)
+        for _ in range(2):   # twice: the ring restarts cleanly on the next launch
+            c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+        c.sync()
+    torch.cuda.synchronize()
+    rows = torch.tensor(sorted({0, 1, 151, 152, 153, M // 2, M - 2, M - 1} & set(range(M))))
+    xs_s = [x[rows].contiguous() for x in xs]
+    ref_ar, ref_ro, ref_no = oracle_fused(xs_s, res[rows].contiguous(), w, wl.eps, len(rows), N, dtype)
+    assert_bits_equal(ar[rows], ref_ar, "ar")
+    assert_bits_equal(ro[rows], ref_ro, "residual_out")
+    assert_norm_close(no[rows], ref_no)
 
 
 def test_fused_aliasing_and_no_ar(car):
@@ -231,8 +271,12 @@ def test_argument_errors_launch_nothing(car):
         assert car.car_reduce_residual_rmsnorm(c.h, [p, p], p, p, -1.0, p, p, None) == car.CAR_ERR_ARG
         assert car.car_ll128_decode_reduce(c.h, [p, p], 7, 0, p) == car.CAR_ERR_ARG
         assert car.car_ll_decode_reduce(c.h, [p, p], 7, 0, p) == car.CAR_ERR_ARG
-        assert car.car_tune_fused(c.h, 3, 64, 1) == car.CAR_ERR_ARG
-        assert car.car_tune_fused(c.h, 1, 48, 1) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, car.CAR_FUSED_ROWS, 3, 64, 1) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, car.CAR_FUSED_ROWS, 1, 48, 1) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, car.CAR_FUSED_PIPELINE, 4, 0, 0) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, car.CAR_FUSED_PIPELINE, 0, 64, 0) == car.CAR_ERR_ARG
+        assert car.car_tune_fused(c.h, 9, 0, 0, 0) == car.CAR_ERR_ARG
+        assert car.car_sync(c.h) == car.CAR_OK
         h = c.h
     assert car.car_destroy(h) == car.CAR_ERR_HANDLE   # already destroyed by the context manager
     assert car.car_reduce(h, [p, p], p) == car.CAR_ERR_HANDLE
