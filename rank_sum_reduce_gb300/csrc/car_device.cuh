@@ -157,6 +157,45 @@ __device__ __forceinline__ void rank_sum(const uint4 (&raw)[W], int n, float (&a
   }
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel waits for the grids it depends
+// on before its first global memory access (so it is correct after any
+// producer), then lets the next PDL-launched kernel of the stream begin its
+// launch and prologue while this grid still runs.  Grids here never exceed
+// the resident CTA count, so the early trigger cannot keep this grid's own
+// CTAs from being scheduled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation (and an optional cluster).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  n++;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    n++;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Stale-line record of one decode: a count and the first kStaleCap pairs.
 constexpr uint32_t kStaleCap = 65536u;  // == CAR_STALE_LIST_MAX
 struct StaleLog {

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int col0 = crank * p.chunk;
   int parity = 0;
+  pdl_wait_and_release();
 
   for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups) {
     const int64_t rbase = row * (int64_t)p.vec_per_row;
@@ -260,9 +261,7 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
   p.chunk = (vec_per_row + sh.cluster - 1) / sh.cluster;
   p.cluster = sh.cluster;
   p.nranks = W;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(sh, s, attr);
-  return cudaLaunchKernelEx(&cfg, fn, p);
+  return launch_pdl(fn, (unsigned)(sh.groups * sh.cluster), (unsigned)sh.threads, 0, s, (unsigned)sh.cluster, p);
 }
 
 }  // namespace car

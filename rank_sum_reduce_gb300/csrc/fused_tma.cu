@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
   }
   __syncthreads();
   if (C > 1) cluster_barrier();  // peers' barriers exist before anyone arrives on them
+  pdl_wait_and_release();        // inputs may come from the previous kernel of the stream
 
   if (warp == nconsumer_warps) {
     if (lane == 0) run_producer(p, ring, full, empty, s_abort, S, slice, n, crank, group, ngroups);
@@ -469,19 +470,8 @@ cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* r
   p.consumers = sh.consumers;
   p.nranks = W;
   p.cluster = sh.cluster;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)sh.grid, 1, 1);
-  cfg.blockDim = dim3((unsigned)(sh.consumers + 32), 1, 1);
-  cfg.dynamicSmemBytes = (size_t)sh.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)sh.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = sh.cluster > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fn, p);
+  return launch_pdl(fn, (unsigned)sh.grid, (unsigned)(sh.consumers + 32), (size_t)sh.smem, s,
+                    (unsigned)sh.cluster, p);
 }
 
 }  // namespace car

@@ -20,6 +20,7 @@ namespace {
 __global__ void __launch_bounds__(kWireThreads)
     ll_encode_kernel(const uint4* __restrict__ data, const int64_t nvec, const uint32_t flag,
                      uint4* __restrict__ wire) {
+  pdl_wait_and_release();
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += step) {
     const uint4 d = ld_stream(data + i);
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(kWireThreads)
                             StaleLog* __restrict__ log) {
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
+  pdl_wait_and_release();
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += step) {
     uint4 raw[R];
@@ -107,17 +109,15 @@ cudaError_t ll_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encod
 
 cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag, void* wire,
                              int grid, cudaStream_t s) {
-  ll_encode_kernel<<<grid, kWireThreads, 0, s>>>(static_cast<const uint4*>(data), data_bytes / 16,
-                                                 flag, static_cast<uint4*>(wire));
-  return cudaGetLastError();
+  return launch_pdl(ll_encode_kernel, (unsigned)grid, kWireThreads, 0, s, 1, static_cast<const uint4*>(data),
+                    data_bytes / 16, flag, static_cast<uint4*>(wire));
 }
 
 cudaError_t launch_ll_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                     uint32_t expected, int max_polls, void* out, StaleLog* log,
                                     int grid, cudaStream_t s) {
-  pick_decode(dtype, W)<<<grid, kWireThreads, 0, s>>>(wires, W, data_bytes / 8, expected, max_polls,
-                                                      static_cast<uint2*>(out), log);
-  return cudaGetLastError();
+  return launch_pdl(pick_decode(dtype, W), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes / 8,
+                    expected, max_polls, static_cast<uint2*>(out), log);
 }
 
 }  // namespace car

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kWireThreads)
   const int lane = threadIdx.x & 31, c = lane & 15;
   const int64_t pairs = (lines + 1) / 2;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait_and_release();
   for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
        wp += nwarps) {
     const int64_t p = 2 * wp + (lane >> 4);
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kWireThreads)
   const int flag_src = lane | 7;
   const int64_t pairs = (lines + 1) / 2;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait_and_release();
   for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
        wp += nwarps) {
     const int64_t p = 2 * wp + (lane >> 4);
@@ -157,17 +159,15 @@ cudaError_t ll128_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* en
 
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
                                 void* wire, int grid, cudaStream_t s) {
-  ll128_encode_kernel<<<grid, kWireThreads, 0, s>>>(static_cast<const uint8_t*>(data), data_bytes,
-                                                    lines, flag, static_cast<uint8_t*>(wire));
-  return cudaGetLastError();
+  return launch_pdl(ll128_encode_kernel, (unsigned)grid, kWireThreads, 0, s, 1, static_cast<const uint8_t*>(data),
+                    data_bytes, lines, flag, static_cast<uint8_t*>(wire));
 }
 
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
                                        StaleLog* log, int grid, cudaStream_t s) {
-  pick_decode(dtype, W)<<<grid, kWireThreads, 0, s>>>(wires, W, data_bytes, lines, expected,
-                                                      max_polls, static_cast<uint8_t*>(out), log);
-  return cudaGetLastError();
+  return launch_pdl(pick_decode(dtype, W), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes, lines,
+                    expected, max_polls, static_cast<uint8_t*>(out), log);
 }
 
 }  // namespace car

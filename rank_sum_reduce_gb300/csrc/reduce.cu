@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kReduceThreads)
                            const int64_t nvec) {
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
+  pdl_wait_and_release();
   const int64_t step = (int64_t)gridDim.x * kReduceThreads * U;
   for (int64_t base = (int64_t)blockIdx.x * kReduceThreads * U + threadIdx.x; base < nvec;
        base += step) {
@@ -87,8 +88,8 @@ cudaError_t reduce_occupancy(int dtype, int W, int* blocks_per_sm) {
 
 cudaError_t launch_reduce(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
                           cudaStream_t s) {
-  pick_reduce(dtype, W)<<<grid, kReduceThreads, 0, s>>>(in, W, static_cast<uint4*>(out), nvec);
-  return cudaGetLastError();
+  return launch_pdl(pick_reduce(dtype, W), (unsigned)grid, kReduceThreads, 0, s, 1, in, W,
+                    static_cast<uint4*>(out), nvec);
 }
 
 }  // namespace car
