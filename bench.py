@@ -39,7 +39,7 @@ HEADLINE = "m512_w8"
 METRIC = "HBM GB/s (fraction of GB300 peak) for W-way reduce+RMSNorm; µs/call at M=1"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
-DOMINANT = "reduce_residual_rmsnorm_tma_kernel"   # the automatic fused kernel at M=512 (M >= 2 x SMs)
+DOMINANT = "reduce_residual_rmsnorm_tma_kernel"   # the automatic fused kernel at M=512 (M >= SM count)
 
 
 # ---------------------------------------------------------------------------

@@ -254,7 +254,7 @@ const char* car_last_error(void);
  * CTA whole rows, 2 splits every row over a CTA pair (needs an even number of
  * 16-byte columns); threads and vpt must be 0; needs N*s <= 100 KiB per CTA.
  * CAR_FUSED_AUTO (all fields 0) restores the automatic choice: the pipeline
- * with whole rows when M >= 2 x the SM count, else rows.
+ * with whole rows when M >= the SM count, else rows.
  * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_SIZE when the shape
  * does not cover a row or the row does not fit the ring. */
 car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int vpt);

@@ -113,12 +113,15 @@ int clamp_grid(int64_t needed, int per_sm, int num_sms) {
 
 int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
 
-// Automatic shape of the fused kernel.
+// Automatic shape of the row-split fused kernel.
 //  * Many rows (M >= 2 x SMs): one CTA per row, the fewest vectors per
 //    thread that the compiled instances allow; split the row over a cluster
 //    only when a single CTA cannot cover it.
-//  * Few rows: split each row over up to 8 CTAs so that about one CTA per SM
-//    is busy, keeping at least 64 vectors per CTA.
+//  * Few rows: split a row over a cluster only while each CTA still pulls
+//    more than about 24 KB of inputs and the SMs are not yet all busy; a
+//    cluster barrier costs about 0.4 us, which a small row cannot repay
+//    (measured on GB300: W=2, N=2048 bf16 runs best on one CTA, W=8,
+//    N=8192 bf16 on eight).
 car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
   car::FusedShape sh{1, 32, 1, 1};
   if (M >= 2 * (int64_t)num_sms) {
@@ -130,8 +133,8 @@ car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
   }
   int c = 1;
   if (M < 2 * (int64_t)num_sms) {
-    while (c < 8 && (int64_t)c * M < num_sms) c *= 2;
-    while (c > 1 && V / c < 64) c /= 2;
+    const int64_t row_input_bytes = (int64_t)(W + 1) * V * 16;
+    while (c < 8 && row_input_bytes / c > 24 * 1024 && (int64_t)c * M < num_sms) c *= 2;
   }
   while (c < 8 && (V + c - 1) / c > car::fused_max_threads(W, 1)) c *= 2;
   sh.cluster = c;
@@ -148,11 +151,11 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
   return (int64_t)sh.threads * sh.vpt >= chunk;
 }
 
-// The pipelined kernel is as fast or faster once every SM streams at least two
-// rows (measured on GB300 at W=8, N=8192 bf16 and W=4, N=4096 fp32); below
-// that the row-split kernel keeps more SMs busy.
+// The pipelined kernel is faster once every SM has a row to stream (measured
+// on GB300 at W=8, N=8192 bf16 and W=4, N=4096 fp32, M >= 304); below that
+// the row-split kernel spreads the few rows over more SMs.
 int auto_fused_kernel(const car_ctx* h) {
-  return (h->tma_ok && h->M >= 2 * (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
+  return (h->tma_ok && h->M >= (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
 }
 
 car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
@@ -282,7 +285,7 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   // The pipelined kernel takes whole rows by default: splitting rows over CTA
   // pairs puts a cross-SM exchange on every row's critical path, which
   // measured slower on GB300 than the quantisation it removes.
-  h->tma_ok = h->fused_ok && car::fused_tma_shape(M, h->vec_per_row, h->num_sms, 1, &h->tma);
+  h->tma_ok = h->fused_ok && car::fused_tma_shape(M, h->vec_per_row, h->num_sms, 1, W, &h->tma);
   h->tma_auto = h->tma;
   if (h->tma_ok && (e = car::fused_tma_prepare(h->dtype, W, h->tma)) != cudaSuccess) return fail(e, "pipeline smem");
   h->fused_kernel_auto = auto_fused_kernel(h);
@@ -345,7 +348,7 @@ car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int 
     if (threads || vpt || (cluster != 0 && cluster != 1 && cluster != 2)) return CAR_ERR_ARG;
     if (!h->tma_ok) return CAR_ERR_SIZE;
     car::FusedTmaShape t;
-    if (!car::fused_tma_shape(h->M, h->vec_per_row, h->num_sms, cluster ? cluster : 1, &t)) return CAR_ERR_SIZE;
+    if (!car::fused_tma_shape(h->M, h->vec_per_row, h->num_sms, cluster ? cluster : 1, h->W, &t)) return CAR_ERR_SIZE;
     cudaError_t e = car::fused_tma_prepare(h->dtype, h->W, t);
     if (e != cudaSuccess) return cuda_fail(e, "pipeline smem");
     h->tma = t;

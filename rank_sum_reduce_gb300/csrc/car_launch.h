@@ -47,7 +47,7 @@ struct FusedTmaShape {
   int smem;       // dynamic shared memory bytes
 };
 // False when the row does not fit the ring design.
-bool fused_tma_shape(int64_t rows, int vec_per_row, int num_sms, int cluster, FusedTmaShape* out);
+bool fused_tma_shape(int64_t rows, int vec_per_row, int num_sms, int cluster, int W, FusedTmaShape* out);
 // Once per shape: allow the kernel instance its dynamic shared memory.
 cudaError_t fused_tma_prepare(int dtype, int W, const FusedTmaShape& sh);
 cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* residual, const void* weight,

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
 
     // 1. all loads of this thread's vectors: W ranks + residual
     uint4 raw[VPT][R];
-    uint4 res[VPT];
+    uint4 res[VPT], wv[VPT];
     bool ok[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
         for (int r = 0; r < R; r++)
           if (r < n) raw[k][r] = ld_stream(static_cast<const uint4*>(p.in.p[r]) + off);
         res[k] = ld_stream(p.residual + off);
+        wv[k] = __ldg(p.weight + col0 + v);  // issued with the inputs: off the statistic's critical path
       }
     }
 
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       if (ok[k]) {
         const int col = col0 + threadIdx.x + k * blockDim.x;
         float wf[E];
-        Pack<DT>::widen(__ldg(p.weight + col), wf);
+        Pack<DT>::widen(wv[k], wf);
         float o[E];
 #pragma unroll
         for (int e = 0; e < E; e++) o[e] = __fmul_rn(__fmul_rn(h[k][e], rms), wf[e]);
