@@ -408,6 +408,34 @@ def timed(torch, fn, iters):
     return e0.elapsed_time(e1) / iters
 
 
+def two_shot_row(arm, iters=200):
+    """Two-shot bit pattern (owner-rotated sum) at the headline shape, graph replay."""
+    torch, car, lib = arm.torch, arm.car, arm.lib
+    wl = workloads.WORKLOADS[HEADLINE]
+    set_bytes = (wl.W + 1) * wl.data_bytes
+    R = n_sets_for(set_bytes)
+    sets = make_sets(torch, wl, arm.dev, R, outputs=("ar",))
+    st, h = car.car_create(wl.W, wl.M, wl.N, car.DTYPE_CODE[wl.dtype])
+    car.check(st, "car_create")
+
+    def fn(S):
+        tbl = Arm.table([x.data_ptr() for x in S["xs"]])
+        ar = S["ar"].data_ptr()
+
+        def run(stream):
+            if lib.car_reduce_two_shot(h, tbl, ar, stream):
+                raise RuntimeError(car.car_last_error())
+        return run
+
+    g = capture(torch, [fn(S) for S in sets])
+    reps = max(1, iters // R)
+    ms = timed(torch, lambda i: g.replay(), reps) / R
+    del g
+    car.check(car.car_destroy(h), "car_destroy")
+    return {"workload": "two_shot_" + wl.name, "ms": round(ms, 4), "bytes": set_bytes,
+            "GBps": round(set_bytes / (ms * 1e-3) / 1e9, 1), "sets": R}
+
+
 def fused_fp32_row(arm, iters=50):
     torch, car = arm.torch, arm.car
     wl = workloads.WORKLOADS["m2048_w4_fp32"]
@@ -595,6 +623,7 @@ def main():
         rows["m1_w2_fused_3out"] = latency_row(arm, workloads.WORKLOADS["m1_w2"], 3)
         rows["m1_w8_fused"] = latency_row(arm, workloads.WORKLOADS["m1_w8"], 2)
         rows["m2048_w4_fp32_fused"] = fused_fp32_row(arm)
+        rows["two_shot_m512_w8"] = two_shot_row(arm)
         rows["ll128_w16_decode_reduce"] = ll128_row(arm)
         rows["ll_m512_w8"] = ll_row(arm)
         torch.cuda.empty_cache()

@@ -116,6 +116,14 @@ car_status car_destroy(car_ctx* h);
  * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG (NULL), CAR_ERR_ALIGN, CAR_ERR_CUDA. */
 car_status car_reduce(car_ctx* h, const void* const* inputs, void* ar_out, void* stream);
 
+/* Two-shot bit pattern (P1 "2stage：分片、轮转、以及为什么没有出口 barrier"):
+ * the same sum as car_reduce, but rounded as a reduce-scatter + all-gather
+ * would round it.  The message's 16-byte units are cut into W shards of
+ * part = units / W (the last shard also takes the remainder; all units when
+ * part == 0), and shard s is summed by its owner in the rotated rank order
+ * s, s+1, ..., s-1.  Arguments, aliasing and errors as car_reduce. */
+car_status car_reduce_two_shot(car_ctx* h, const void* const* inputs, void* ar_out, void* stream);
+
 /* ---------------------------------------------------------------------- */
 /* Fused rank sum + residual add + RMSNorm                                 */
 /* (P4 "这个算子在算什么" and "总体设计")                                   */

@@ -63,6 +63,7 @@ def _load():
             "orc_elem_size": (ctypes.c_int, [ctypes.c_int]),
             "orc_convert": (None, [vp, ctypes.c_int, vp, ctypes.c_int, i64]),
             "orc_reduce": (None, [ctypes.c_int, pvp, ctypes.c_int, i64, vp]),
+            "orc_reduce_two_shot": (None, [ctypes.c_int, pvp, ctypes.c_int, i64, vp]),
             "orc_reduce_residual_rmsnorm": (None, [ctypes.c_int, pvp, vp, vp, ctypes.c_float, i64, i64,
                                                    ctypes.c_int, vp, vp, vp, vp]),
             "orc_ll128_lines": (i64, [i64]),
@@ -138,6 +139,20 @@ def reduce(xs, dtype: str, out) -> None:
             raise ValueError("buffer too small")
     tbl, keep = _ptr_table(xs)
     _load().orc_reduce(len(xs), tbl, DTYPE_CODE[dtype], n, _ptr(out))
+    del keep
+
+
+def reduce_two_shot(xs, dtype: str, out) -> None:
+    """Two-shot bit pattern: each shard summed in its owner's rotated rank order."""
+    es = ELEM_SIZE[dtype]
+    n = _nbytes(xs[0]) // es
+    if (n * es) % 16:
+        raise ValueError("message bytes must be a multiple of 16")
+    for a in list(xs) + [out]:
+        if _nbytes(a) < n * es:
+            raise ValueError("buffer too small")
+    tbl, keep = _ptr_table(xs)
+    _load().orc_reduce_two_shot(len(xs), tbl, DTYPE_CODE[dtype], n, _ptr(out))
     del keep
 
 

@@ -254,6 +254,31 @@ void orc_reduce(int W, const void* const* x, int dtype, int64_t n, void* ar) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* P1 "2stage：分片、轮转、以及为什么没有出口 barrier": stage 1 gives rank s  */
+/* the units [s*part, (s+1)*part) (the last rank up to the end) and rank s   */
+/* reads the ranks starting from itself, (s + i) % W.  All ranks then gather */
+/* the owner's result, so every element carries its owner's rounding.        */
+/* ------------------------------------------------------------------------ */
+void orc_reduce_two_shot(int W, const void* const* x, int dtype, int64_t n, void* ar) {
+  const int es = orc_elem_size(dtype);
+  if ((n * es) % 16 != 0) return;
+  const int64_t units = n * es / 16;
+  const int64_t per_unit = 16 / es;
+  const int64_t part = units / W;
+  for (int64_t i = 0; i < n; i++) {
+    const int64_t unit = i / per_unit;
+    int64_t owner = part == 0 ? W - 1 : unit / part;
+    if (owner > W - 1) owner = W - 1;  /* the last rank takes the remainder */
+    float acc = load_elem((const uint8_t*)x[owner] + i * es, dtype);
+    for (int k = 1; k < W; k++) {
+      const int r = (int)((owner + k) % W);
+      acc = acc + load_elem((const uint8_t*)x[r] + i * es, dtype);
+    }
+    store_from_f32((uint8_t*)ar + i * es, dtype, acc);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* P4 "这个算子在算什么":                                                     */
 /*   ar = sum over ranks of x;  h = ar + residual  (-> residual_out)        */
 /*   rms = rsqrt(mean(h^2) + eps);  out = (h * rms) * weight (-> norm_out)   */

@@ -43,6 +43,14 @@ void     orc_convert(const void* src, int src_kind, void* dst, int dst_kind, int
  *      with every "+" an fp32 add, seeded with x_0. n = element count. ---- */
 void orc_reduce(int W, const void* const* x, int dtype, int64_t n, void* ar);
 
+/* ---- two-shot bit pattern: P1 "2stage：分片、轮转、以及为什么没有出口 barrier".
+ *      The message's 16-byte packed units are cut into W shards of
+ *      part = units / W units; the last shard also takes the remainder (all
+ *      units when part == 0).  Shard s is summed by its owner in the rotated
+ *      order s, s+1, ..., s-1 (mod W), fp32, one rounding.  n * elem_size must
+ *      be a multiple of 16 (otherwise nothing is written). ---- */
+void orc_reduce_two_shot(int W, const void* const* x, int dtype, int64_t n, void* ar);
+
 /* ---- fused reduce + residual + RMSNorm: P4 "这个算子在算什么".
  *      Row-major [M,N].  ar (nullable), residual_out, norm_out have type
  *      dtype; norm_f64 (nullable, M*N doubles) receives the unrounded value.

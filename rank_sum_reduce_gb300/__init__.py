@@ -48,6 +48,7 @@ _SIGS = {
     "car_create": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _ctx_pp]),
     "car_destroy": (ctypes.c_int, [_vp]),
     "car_reduce": (ctypes.c_int, [_vp, _pvp, _vp, _vp]),
+    "car_reduce_two_shot": (ctypes.c_int, [_vp, _pvp, _vp, _vp]),
     "car_reduce_residual_rmsnorm": (ctypes.c_int, [_vp, _pvp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]),
     "car_ll128_wire_bytes": (ctypes.c_size_t, [_vp]),
     "car_ll128_encode": (ctypes.c_int, [_vp, _vp, ctypes.c_uint64, _vp, _vp]),
@@ -98,6 +99,10 @@ def car_destroy(h) -> int:
 
 def car_reduce(h, inputs, ar_out: int, stream: int = 0) -> int:
     return _lib.car_reduce(h, _table(inputs) if inputs is not None else None, ar_out, stream)
+
+
+def car_reduce_two_shot(h, inputs, ar_out: int, stream: int = 0) -> int:
+    return _lib.car_reduce_two_shot(h, _table(inputs) if inputs is not None else None, ar_out, stream)
 
 
 def car_reduce_residual_rmsnorm(h, inputs, residual: int, weight: int, eps: float, residual_out: int,
@@ -231,6 +236,10 @@ class Car:
 
     def reduce(self, xs, ar_out, stream=None):
         check(car_reduce(self.h, [x.data_ptr() for x in xs], ar_out.data_ptr(), _stream(stream)), "car_reduce")
+
+    def reduce_two_shot(self, xs, ar_out, stream=None):
+        check(car_reduce_two_shot(self.h, [x.data_ptr() for x in xs], ar_out.data_ptr(), _stream(stream)),
+              "car_reduce_two_shot")
 
     def reduce_residual_rmsnorm(self, xs, residual, weight, eps, residual_out, norm_out, ar_out=None, stream=None):
         check(car_reduce_residual_rmsnorm(self.h, [x.data_ptr() for x in xs], residual.data_ptr(),

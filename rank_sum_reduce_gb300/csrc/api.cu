@@ -39,6 +39,7 @@ struct car_ctx {
   int device;
   int num_sms;
   int reduce_grid;
+  int two_shot_grid;
   bool fused_ok;        // row short enough for the fused kernel
   car::FusedShape fused_auto;
   car::FusedShape fused;
@@ -269,6 +270,8 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   if ((e = car::reduce_occupancy(h->dtype, W, &per_sm)) != cudaSuccess) return fail(e, "reduce occupancy");
   const int64_t per_cta = (int64_t)car::kReduceThreads * car::reduce_vectors_per_thread(W);
   h->reduce_grid = clamp_grid((h->nvec + per_cta - 1) / per_cta, per_sm, h->num_sms);
+  if ((e = car::two_shot_occupancy(h->dtype, W, &per_sm)) != cudaSuccess) return fail(e, "two-shot occupancy");
+  h->two_shot_grid = clamp_grid((h->nvec + per_cta - 1) / per_cta, per_sm, h->num_sms);
 
   if ((e = car::ll128_occupancy(h->dtype, W, &per_sm, &per_sm2)) != cudaSuccess) return fail(e, "ll128 occupancy");
   const int64_t pairs = (h->ll128_lines + 1) / 2;
@@ -392,6 +395,17 @@ car_status car_reduce(car_ctx* h, const void* const* inputs, void* ar_out, void*
   cudaError_t e = car::launch_reduce(h->dtype, h->W, tbl, ar_out, h->nvec, h->reduce_grid,
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "rank_sum_reduce launch");
+}
+
+car_status car_reduce_two_shot(car_ctx* h, const void* const* inputs, void* ar_out, void* stream) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  car::RankPtrs tbl;
+  if ((st = check_table(h, inputs, &tbl)) != CAR_OK) return st;
+  if ((st = check_dev(ar_out)) != CAR_OK) return st;
+  cudaError_t e = car::launch_two_shot(h->dtype, h->W, tbl, ar_out, h->nvec, h->two_shot_grid,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "rank_sum_two_shot launch");
 }
 
 car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, const void* residual,

@@ -18,6 +18,10 @@ int reduce_vectors_per_thread(int W);
 cudaError_t reduce_occupancy(int dtype, int W, int* blocks_per_sm);
 cudaError_t launch_reduce(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
                           cudaStream_t s);
+// two-shot bit pattern: shard s of the nvec units summed from rank s onwards
+cudaError_t two_shot_occupancy(int dtype, int W, int* blocks_per_sm);
+cudaError_t launch_two_shot(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
+                            cudaStream_t s);
 
 // ---- fused rank sum + residual + RMSNorm (fused.cu) ----
 struct FusedShape {

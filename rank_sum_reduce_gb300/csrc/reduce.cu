@@ -49,7 +49,59 @@ __global__ void __launch_bounds__(kReduceThreads)
   }
 }
 
+// Two-shot bit pattern (P1 "2stage：分片、轮转、以及为什么没有出口 barrier"):
+// the 16-byte units are cut into W shards of `part` units (the last shard
+// takes the remainder, and everything when part == 0); shard s is summed in
+// the rotated order s, s+1, ..., s-1.  On one GPU there is nothing to
+// scatter or gather: the kernel reproduces the owner's rounding in one pass.
+template <int DT, int W, int U>
+__global__ void __launch_bounds__(kReduceThreads)
+    rank_sum_two_shot_kernel(const RankPtrs in, const int nranks, uint4* __restrict__ out,
+                             const int64_t nvec, const int64_t part) {
+  constexpr int R = W > 0 ? W : kMaxRanks;
+  const int n = W > 0 ? W : nranks;
+  // the pointer table, indexed by a per-vector rank: shared memory instead of a local copy
+  __shared__ const uint4* s_ptr[kMaxRanks];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; r++) s_ptr[r] = static_cast<const uint4*>(in.p[r]);
+  }
+  __syncthreads();
+  pdl_wait_and_release();
+  const int64_t step = (int64_t)gridDim.x * kReduceThreads * U;
+  for (int64_t base = (int64_t)blockIdx.x * kReduceThreads * U + threadIdx.x; base < nvec;
+       base += step) {
+    uint4 raw[U][R];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t v = base + (int64_t)u * kReduceThreads;
+      if (v < nvec) {
+        int owner = n - 1;
+        if (part > 0 && v / part < n - 1) owner = (int)(v / part);
+#pragma unroll
+        for (int i = 0; i < R; i++) {
+          if (i < n) {
+            int r = owner + i;
+            if (r >= n) r -= n;
+            raw[u][i] = ld_stream(s_ptr[r] + v);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t v = base + (int64_t)u * kReduceThreads;
+      if (v < nvec) {
+        float acc[Pack<DT>::kN];
+        rank_sum<DT, R>(raw[u], n, acc);
+        st16(out + v, Pack<DT>::narrow(acc));
+      }
+    }
+  }
+}
+
 using ReduceFn = void (*)(const RankPtrs, const int, uint4*, const int64_t);
+using TwoShotFn = void (*)(const RankPtrs, const int, uint4*, const int64_t, const int64_t);
 
 // Vectors per thread per iteration: enough loads in flight per thread without
 // spilling (about 8 to 16 outstanding 16-byte loads).
@@ -64,6 +116,26 @@ ReduceFn pick(int W) {
     case 8: return rank_sum_reduce_kernel<DT, 8, vectors_for(8)>;
     case 16: return rank_sum_reduce_kernel<DT, 16, vectors_for(16)>;
     default: return rank_sum_reduce_kernel<DT, 0, 1>;
+  }
+}
+
+template <int DT>
+TwoShotFn pick2(int W) {
+  switch (W) {
+    case 1: return rank_sum_two_shot_kernel<DT, 1, vectors_for(1)>;
+    case 2: return rank_sum_two_shot_kernel<DT, 2, vectors_for(2)>;
+    case 4: return rank_sum_two_shot_kernel<DT, 4, vectors_for(4)>;
+    case 8: return rank_sum_two_shot_kernel<DT, 8, vectors_for(8)>;
+    case 16: return rank_sum_two_shot_kernel<DT, 16, vectors_for(16)>;
+    default: return rank_sum_two_shot_kernel<DT, 0, 1>;
+  }
+}
+
+TwoShotFn pick_two_shot(int dtype, int W) {
+  switch (dtype) {
+    case kBF16: return pick2<kBF16>(W);
+    case kFP16: return pick2<kFP16>(W);
+    default: return pick2<kFP32>(W);
   }
 }
 
@@ -84,6 +156,17 @@ int reduce_vectors_per_thread(int W) {
 cudaError_t reduce_occupancy(int dtype, int W, int* blocks_per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       blocks_per_sm, reinterpret_cast<const void*>(pick_reduce(dtype, W)), kReduceThreads, 0);
+}
+
+cudaError_t two_shot_occupancy(int dtype, int W, int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      blocks_per_sm, reinterpret_cast<const void*>(pick_two_shot(dtype, W)), kReduceThreads, 0);
+}
+
+cudaError_t launch_two_shot(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,
+                            cudaStream_t s) {
+  return launch_pdl(pick_two_shot(dtype, W), (unsigned)grid, kReduceThreads, 0, s, 1, in, W,
+                    static_cast<uint4*>(out), nvec, nvec / W);
 }
 
 cudaError_t launch_reduce(int dtype, int W, const RankPtrs& in, void* out, int64_t nvec, int grid,

@@ -69,6 +69,7 @@ def test_calls_on_bad_handles(car):
     assert car.car_destroy(None) == car.CAR_ERR_HANDLE
     assert car.car_destroy(bogus) == car.CAR_ERR_HANDLE
     assert car.car_reduce(bogus, [0x10], 0x10) == car.CAR_ERR_HANDLE
+    assert car.car_reduce_two_shot(bogus, [0x10], 0x10) == car.CAR_ERR_HANDLE
     assert car.car_reduce_residual_rmsnorm(bogus, [0x10], 16, 16, 1e-6, 16, 16, None) == car.CAR_ERR_HANDLE
     assert car.car_ll128_encode(bogus, 16, 7, 16) == car.CAR_ERR_HANDLE
     assert car.car_ll128_decode_reduce(bogus, [16], 7, 1, 16) == car.CAR_ERR_HANDLE

@@ -579,3 +579,70 @@ def test_stale_list_cap(orc):
     n, lst = orc.ll128_decode_reduce([wire, wire], D, "bf16", 4, out, cap=7)
     assert n == 20 and lst.shape == (7, 2)
     assert lst.tolist() == [[r, k] for k in range(10) for r in range(2)][:7]
+
+
+# ----------------------------------------------------------------------------
+# two-shot bit pattern  (P1 "2stage：分片、轮转、以及为什么没有出口 barrier")
+# ----------------------------------------------------------------------------
+def _owners(orc, W, units, probe_units):
+    """For each probed unit, the ranks r such that the plain rank sum taken in
+    the order r, r+1, ..., r-1 reproduces the two-shot result there.  fp32
+    inputs spread over many binades make the order visible in the rounding;
+    candidates are intersected over several independent draws."""
+    n = units * 4
+    owners = {u: set(range(W)) for u in probe_units}
+    for seed in range(6):
+        rng = np.random.default_rng(12345 + seed)
+        xs = [(rng.standard_normal(n) * np.exp2(rng.integers(-12, 13, n))).astype(np.float32) for _ in range(W)]
+        out = np.empty(n, dtype=np.float32)
+        orc.reduce_two_shot(xs, "fp32", out)
+        for u in probe_units:
+            sl = slice(u * 4, (u + 1) * 4)
+            for r in list(owners[u]):
+                want = np.empty(4, dtype=np.float32)
+                orc.reduce([xs[(r + k) % W][sl].copy() for k in range(W)], "fp32", want)
+                if not np.array_equal(want.view(np.uint32), out[sl].view(np.uint32)):
+                    owners[u].discard(r)
+    return {u: sorted(c) for u, c in owners.items()}
+
+
+def test_two_shot_shards_match_the_page(orc):
+    """page value: a 512 KB message over 8 ranks has part = 4096 units; the
+    owner (first rank of the sum) changes at unit 4096; the last rank owns the
+    remainder."""
+    (case,) = read_golden("two_shot_shards.txt")
+    W, units = int(case["W"]), int(case["units"])
+    assert int(case["message_bytes"]) // 16 == units and units // W == int(case["part"])
+    keys = ("4095", "4096", "32767")
+    owners = _owners(orc, W, units, [int(k) for k in keys])
+    for key in keys:
+        assert owners[int(key)] == [int(case[f"owner_of_unit_{key}"])]
+
+
+@pytest.mark.parametrize("W,units", [(1, 7), (3, 10), (4, 2), (5, 23), (8, 8), (16, 40)])
+def test_two_shot_is_rotated_one_shot_per_shard(orc, W, units):
+    """closed form: each shard equals the plain rank sum over the rank list
+    rotated to start at its owner; part = 0 gives everything to the last rank."""
+    rng = np.random.default_rng(W * 100 + units)
+    n = units * 8
+    xs = [_bf16(rng.standard_normal(n) * 10.0 ** rng.integers(-3, 4)) for _ in range(W)]
+    out = np.empty(n, dtype=np.uint16)
+    orc.reduce_two_shot(xs, "bf16", out)
+    part = units // W
+    for u in range(units):
+        owner = W - 1 if part == 0 else min(u // part, W - 1)
+        rot = [xs[(owner + k) % W][u * 8:(u + 1) * 8].copy() for k in range(W)]
+        want = np.empty(8, dtype=np.uint16)
+        orc.reduce(rot, "bf16", want)
+        assert np.array_equal(out[u * 8:(u + 1) * 8], want)
+
+
+def test_two_shot_equals_one_shot_on_exact_inputs(orc):
+    """closed form: integer-valued inputs sum exactly in any order."""
+    rng = np.random.default_rng(9)
+    W, n = 6, 6000
+    xs = [rng.integers(-256, 257, n).astype(np.float32) for _ in range(W)]
+    a, b = np.empty(n, dtype=np.float32), np.empty(n, dtype=np.float32)
+    orc.reduce(xs, "fp32", a)
+    orc.reduce_two_shot(xs, "fp32", b)
+    assert np.array_equal(a, b)

@@ -98,6 +98,22 @@ def test_reduce_bit_exact(car, W, M, N, dtype):
     assert_bits_equal(out, oracle_reduce(xs, dtype), "ar")
 
 
+@pytest.mark.parametrize("W,M,N,dtype", REDUCE_CASES + [(8, 512, 8192, "bf16"), (3, 1, 8, "bf16"), (16, 1, 64, "fp32")])
+def test_two_shot_bit_exact(car, W, M, N, dtype):
+    """Owner-rotated sums, including part == 0 (fewer units than ranks) and a
+    remainder for the last shard."""
+    wl = workloads.custom(W, M, N, dtype, seed=7000 + W * 7 + M)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    dx = [x.to(DEV) for x in xs]
+    out = torch.full_like(dx[0], float("nan"))
+    with car.Car(W, M, N, dtype) as c:
+        c.reduce_two_shot(dx, out)
+    torch.cuda.synchronize()
+    want = torch.empty_like(xs[0])
+    oracle.reduce_two_shot(xs, dtype, want)
+    assert_bits_equal(out, want, "two-shot ar")
+
+
 def test_reduce_output_may_alias_an_input(car):
     W, M, N = 8, 19, 1032
     wl = workloads.custom(W, M, N, "bf16", seed=5)
@@ -461,3 +477,78 @@ def test_ll128_workload_full_size(car):
         got = out.view(-1)[d0 // 2: d1 // 2].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got, ref)
         assert {(int(r), int(k) + k0) for r, k in lst} == {(r, k) for r, k in planted if k0 <= k < k1}
+
+
+# ---------------------------------------------------------------------------
+# launch ordering: programmatic dependent launch and CUDA-graph capture
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 3, 200])
+def test_chained_calls_see_previous_outputs(car, M):
+    """Back-to-back calls where each call's residual is the previous call's
+    residual_out (and its rank 0 input the previous ar): every kernel waits
+    for its predecessor before reading, so the chain equals the oracle chain."""
+    W, N, steps = 4, 2048, 4
+    wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=900 + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    outs = [(torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)) for _ in range(steps)]
+    with car.Car(W, M, N, "bf16") as c:
+        cur_res, cur_x0 = dres, dx[0]
+        for k in range(steps):
+            ro, no, ar = outs[k]
+            c.reduce_residual_rmsnorm([cur_x0] + dx[1:], cur_res, dw, wl.eps, ro, no, ar)
+            cur_res, cur_x0 = ro, ar
+        c.sync()
+    torch.cuda.synchronize()
+    ref_res, ref_x0 = res, xs[0]
+    for k in range(steps):
+        ref_ar, ref_ro, ref_no = oracle_fused([ref_x0] + xs[1:], ref_res, w, wl.eps, M, N, "bf16")
+        ro, no, ar = outs[k]
+        assert_bits_equal(ar, ref_ar, f"ar step {k}")
+        assert_bits_equal(ro, ref_ro, f"residual_out step {k}")
+        assert_norm_close(no, ref_no, f"norm_out step {k}")
+        ref_res, ref_x0 = ref_ro, ref_ar
+
+
+@pytest.mark.parametrize("M", [1, 400])
+def test_graph_capture_replays_correctly(car, M):
+    """Capture reduce + fused + LL128 encode/decode in one CUDA graph, change
+    the inputs in place, replay: outputs follow the new inputs."""
+    W, N = 8, 1024
+    wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=1300 + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    ar, ro, no, dec = (torch.empty_like(dres) for _ in range(4))
+    c = car.Car(W, M, N, "bf16")
+    wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+
+    def body(stream):
+        c.reduce(dx, ar, stream=stream)
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, stream=stream)
+        for x, wv in zip(dx, wires):
+            c.ll128_encode(x, 11, wv, stream=stream)
+        c.ll128_decode_reduce(wires, 11, dec, stream=stream)
+
+    with torch.cuda.stream(side):
+        body(side.cuda_stream)
+        side.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            body(torch.cuda.current_stream().cuda_stream)
+    for trial in range(2):
+        new = workloads.make_inputs(workloads.custom(W, M, N, "bf16", seed=1400 + trial), "cpu")
+        for d, h in zip(dx, new[0]):
+            d.copy_(h)
+        dres.copy_(new[1])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref_ar, ref_ro, ref_no = oracle_fused(new[0], new[1], w, wl.eps, M, N, "bf16")
+        assert_bits_equal(ar, ref_ar, "ar (graph)")
+        assert_bits_equal(dec, ref_ar, "LL128 decode (graph)")
+        assert_bits_equal(ro, ref_ro, "residual_out (graph)")
+        assert_norm_close(no, ref_no, "norm_out (graph)")
+    assert c.ll128_report()[0] == 0
+    c.sync()
+    c.close()
