@@ -624,17 +624,17 @@ def test_two_shot_is_rotated_one_shot_per_shard(orc, W, units):
     """closed form: each shard equals the plain rank sum over the rank list
     rotated to start at its owner; part = 0 gives everything to the last rank."""
     rng = np.random.default_rng(W * 100 + units)
-    n = units * 8
-    xs = [_bf16(rng.standard_normal(n) * 10.0 ** rng.integers(-3, 4)) for _ in range(W)]
-    out = np.empty(n, dtype=np.uint16)
-    orc.reduce_two_shot(xs, "bf16", out)
+    n = units * 4   # fp32: 4 elements per 16-byte unit, spread over many binades so order shows
+    xs = [(rng.standard_normal(n) * np.exp2(rng.integers(-12, 13, n))).astype(np.float32) for _ in range(W)]
+    out = np.empty(n, dtype=np.float32)
+    orc.reduce_two_shot(xs, "fp32", out)
     part = units // W
     for u in range(units):
         owner = W - 1 if part == 0 else min(u // part, W - 1)
-        rot = [xs[(owner + k) % W][u * 8:(u + 1) * 8].copy() for k in range(W)]
-        want = np.empty(8, dtype=np.uint16)
-        orc.reduce(rot, "bf16", want)
-        assert np.array_equal(out[u * 8:(u + 1) * 8], want)
+        rot = [xs[(owner + k) % W][u * 4:(u + 1) * 4].copy() for k in range(W)]
+        want = np.empty(4, dtype=np.float32)
+        orc.reduce(rot, "fp32", want)
+        assert np.array_equal(out[u * 4:(u + 1) * 4].view(np.uint32), want.view(np.uint32))
 
 
 def test_two_shot_equals_one_shot_on_exact_inputs(orc):
@@ -646,3 +646,29 @@ def test_two_shot_equals_one_shot_on_exact_inputs(orc):
     orc.reduce(xs, "fp32", a)
     orc.reduce_two_shot(xs, "fp32", b)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("kind", ["fp32", "bf16"])
+def test_reduce_is_sequential_fp32_adds_in_rank_order(orc, kind):
+    """independent formulation: numpy float32 adds (IEEE binary32, round to
+    nearest even), applied rank by rank from rank 0, then the library's
+    rounding to the element type.  Values spread over many binades make the
+    rank order visible in the rounding, so a reordered sum fails here."""
+    rng = np.random.default_rng(77)
+    W, n = 8, 20000
+    f = [(rng.standard_normal(n) * np.exp2(rng.integers(-10, 11, n))).astype(np.float32) for _ in range(W)]
+    xs = f if kind == "fp32" else [torch_bf16_bits(v) for v in f]
+    vals = f if kind == "fp32" else [widen(b, "bf16") for b in xs]
+    acc = vals[0].copy()
+    for r in range(1, W):
+        acc = (acc + vals[r]).astype(np.float32)
+    out = np.empty_like(xs[0])
+    orc.reduce(xs, kind, out)
+    if kind == "fp32":
+        assert np.array_equal(out.view(np.uint32), acc.view(np.uint32))
+    else:
+        assert np.array_equal(out, torch_bf16_bits(acc))
+    rev = acc = vals[W - 1].copy()
+    for r in range(W - 2, -1, -1):
+        rev = (rev + vals[r]).astype(np.float32)
+    assert not np.array_equal(rev.view(np.uint32), out.view(np.uint32) if kind == "fp32" else widen(out, kind).view(np.uint32))
