@@ -510,14 +510,24 @@ def barrier(world):
 
 
 def max_over_ranks(value, world):
+    """The largest of every rank's value (timing only; not on the data path)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(region_ms_local, steps, step_bytes, world):
+    """Weak scaling: every rank runs `steps` steps of its own replica.  The
+    job's time is the slowest rank's; value counts the bytes of all ranks."""
+    region_ms = max_over_ranks(region_ms_local, world)
+    ms_per_step = region_ms / steps
+    return ms_per_step, world * step_bytes / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -636,10 +646,8 @@ def main():
     if sampler:
         time.sleep(0.3)
         sampler.stop()
-    region_ms = max_over_ranks(H["region_ms"], world)
     step_bytes = bytes_reduce(wl) + bytes_fused(wl, 2)
-    ms_per_step = region_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = aggregate(H["region_ms"], args.steps, step_bytes, world)
 
     e2e_steps = max(3, min(args.steps, 50))
     e2e_ms, h2d, d2h = e2e(arm, wl, e2e_steps, 3)
