@@ -436,6 +436,38 @@ def two_shot_row(arm, iters=200):
             "GBps": round(set_bytes / (ms * 1e-3) / 1e9, 1), "sets": R}
 
 
+def lamport_row(arm, wl, rounds=30, reps=20):
+    """Lamport one-shot push at M=1: µs per receive (fused residual + RMSNorm,
+    sentinel checks and refill of the previous region) and µs per round (W
+    pushes + the receive), from graph replay; small enough to stay in L2."""
+    torch, car = arm.torch, arm.car
+    c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
+    comm = torch.empty(c.lamport_buffer_bytes, dtype=torch.uint8, device=arm.dev)
+    xs, res, w = workloads.make_inputs(wl, arm.dev)
+    ro, no = torch.empty_like(res), torch.empty_like(res)
+    c.lamport_init(comm)
+
+    def round_fn(j, push):
+        def run(stream):
+            if push:
+                for r, x in enumerate(xs):
+                    c.lamport_push(x, r, j, comm, stream=stream)
+            c.lamport_reduce_residual_rmsnorm(comm, j, res, w, wl.eps, ro, no, stream=stream)
+        return run
+
+    full = capture(torch, [round_fn(j, True) for j in range(rounds)])
+    recv = capture(torch, [round_fn(j, False) for j in range(rounds)])
+    full.replay()
+    n_stale, _ = c.lamport_report()
+    per_round = timed(torch, lambda i: full.replay(), reps) * 1000.0 / rounds
+    per_recv = timed(torch, lambda i: recv.replay(), reps) * 1000.0 / rounds
+    del full, recv
+    c.close()
+    return {"workload": "lamport_" + wl.name, "us_per_receive": round(per_recv, 3),
+            "us_per_round_with_pushes": round(per_round, 3), "kernels_per_round": wl.W + 1,
+            "stale_after_full_round": n_stale, "l2": "warm (buffers fit in L2)"}
+
+
 def fused_fp32_row(arm, iters=50):
     torch, car = arm.torch, arm.car
     wl = workloads.WORKLOADS["m2048_w4_fp32"]
@@ -632,6 +664,8 @@ def main():
     if not args.no_rows and rank == 0:
         rows["m1_w2_fused_3out"] = latency_row(arm, workloads.WORKLOADS["m1_w2"], 3)
         rows["m1_w8_fused"] = latency_row(arm, workloads.WORKLOADS["m1_w8"], 2)
+        rows["lamport_m1_w2"] = lamport_row(arm, workloads.WORKLOADS["m1_w2"])
+        rows["lamport_m1_w8"] = lamport_row(arm, workloads.WORKLOADS["m1_w8"])
         rows["m2048_w4_fp32_fused"] = fused_fp32_row(arm)
         rows["two_shot_m512_w8"] = two_shot_row(arm)
         rows["ll128_w16_decode_reduce"] = ll128_row(arm)

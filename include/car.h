@@ -243,6 +243,45 @@ car_status car_ll_decode_reduce(car_ctx* h, const void* const* wires, uint32_t e
 car_status car_ll_report(car_ctx* h, car_stale_report* out);
 
 /* ---------------------------------------------------------------------- */
+/* Lamport one-shot push, bf16 (P4 "方案二：Lamport（负零轮询）")           */
+/* ---------------------------------------------------------------------- */
+/* The data itself signals arrival: two bf16 share a 32-bit word, the
+ * receive buffer starts filled with the sentinel word 0x80008000 (two
+ * bf16 -0.0), and senders turn -0.0 into +0.0 so that real data never equals
+ * it.  Buffers rotate over three regions: round k uses region k % 3 and its
+ * receive step refills region (k + 2) % 3, the one round k - 1 used.
+ *
+ * The receive buffer `comm` (dev, car_lamport_buffer_bytes(h) bytes) holds
+ * 3 regions x W slots x D bytes; slot r of region k starts at byte
+ * (k * W + r) * D.  The handle's dtype must be bf16 (CAR_ERR_ARG otherwise). */
+
+/* 3 * W * D bytes; 0 for an invalid handle or a dtype other than bf16. */
+size_t car_lamport_buffer_bytes(car_ctx* h);
+
+/* Fill all three regions with the sentinel (once, before the first round). */
+car_status car_lamport_init(car_ctx* h, void* comm, void* stream);
+
+/* Rank `rank` (0..W-1) sends its [M, N] bf16 data for round `round`: the data,
+ * with -0.0 turned into +0.0, goes to slot `rank` of region round % 3. */
+car_status car_lamport_push(car_ctx* h, const void* data, int rank, uint64_t round, void* comm, void* stream);
+
+/* Receive round `round` and apply the fused op: every word of region
+ * round % 3 is checked against the sentinel on the load that reads it; a
+ * missing word is re-read at most max_polls - 1 more times.  Rows complete in
+ * every rank get the rank sum (rank order, fp32) + residual + RMSNorm exactly
+ * as car_reduce_residual_rmsnorm computes it on the pushed values; rows with
+ * a word still missing in some rank are written as 0 (ar, residual_out,
+ * norm_out) and every such (rank, row) is recorded for car_lamport_report.
+ * Region (round + 2) % 3 is refilled with the sentinel in the same pass.
+ * Arguments as car_reduce_residual_rmsnorm; max_polls >= 1. */
+car_status car_lamport_reduce_residual_rmsnorm(car_ctx* h, void* comm, uint64_t round, int max_polls,
+                                               const void* residual, const void* weight, float eps,
+                                               void* residual_out, void* norm_out, void* ar_out, void* stream);
+
+/* Stale (rank, row) pairs of the last Lamport receive, as car_ll128_report. */
+car_status car_lamport_report(car_ctx* h, car_stale_report* out);
+
+/* ---------------------------------------------------------------------- */
 /* Diagnostics                                                              */
 /* ---------------------------------------------------------------------- */
 

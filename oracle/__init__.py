@@ -69,6 +69,10 @@ def _bind(lib):
         "orc_ll_data_capacity": (i64, [i64]),
         "orc_ll_encode": (None, [vp, i64, u32, vp]),
         "orc_ll_decode_reduce": (i64, [ctypes.c_int, pvp, i64, ctypes.c_int, u32, vp, vp, i64]),
+        "orc_lamport_fill": (None, [vp, i64]),
+        "orc_lamport_push": (None, [vp, i64, vp]),
+        "orc_lamport_reduce_residual_rmsnorm": (i64, [ctypes.c_int, vp, u64, i64, i64, vp, vp, ctypes.c_float,
+                                                      vp, vp, vp, vp, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -239,6 +243,33 @@ class Oracle:
         if _nbytes(out) < data_bytes:
             raise ValueError("output too small")
         return self._decode(self._lib.orc_ll_decode_reduce, wires, data_bytes, dtype, expected_flag, out, cap)
+
+    # Lamport one-shot push (bf16)
+    LAMPORT_SENTINEL = 0x80008000
+
+    def lamport_buffer_bytes(self, W: int, n: int) -> int:
+        return 3 * W * n * 2
+
+    def lamport_fill(self, words) -> None:
+        self._lib.orc_lamport_fill(_ptr(words), _nbytes(words) // 4)
+
+    def lamport_push(self, data, n: int, buffer, W: int, rank: int, round_: int) -> None:
+        """Push rank's n bf16 values into its slot of region round % 3."""
+        if _nbytes(buffer) < self.lamport_buffer_bytes(W, n) or _nbytes(data) < 2 * n:
+            raise ValueError("buffer too small")
+        off = ((round_ % 3) * W + rank) * n * 2
+        self._lib.orc_lamport_push(_ptr(data), n, _ptr(buffer) + off)
+
+    def lamport_reduce_residual_rmsnorm(self, W: int, buffer, round_: int, M: int, N: int, residual, weight,
+                                        eps: float, residual_out, norm_out, ar_out=None, cap: int = 1 << 16):
+        """Returns (n_stale, stale[k] = (rank, row))."""
+        if _nbytes(buffer) < self.lamport_buffer_bytes(W, M * N):
+            raise ValueError("buffer too small")
+        stale = np.zeros((max(cap, 1), 2), dtype=np.uint32)
+        n = self._lib.orc_lamport_reduce_residual_rmsnorm(
+            W, _ptr(buffer), round_, M, N, _ptr(residual), _ptr(weight), ctypes.c_float(eps),
+            _ptr(ar_out) if ar_out is not None else None, _ptr(residual_out), _ptr(norm_out), stale.ctypes.data, cap)
+        return int(n), stale[: min(int(n), cap)]
 
     # conversions (used by the pins)
     def convert(self, src: np.ndarray, src_kind: str, dst_kind: str) -> np.ndarray:

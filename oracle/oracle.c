@@ -431,3 +431,64 @@ int64_t orc_ll_decode_reduce(int W, const void* const* wires, int64_t D, int dty
   }
   return n_stale;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Lamport one-shot push, P4 "方案二：Lamport（负零轮询）": two bf16 share a  */
+/* 32-bit word (the low half holds the even element), the buffer starts as   */
+/* sentinel words 0x80008000, senders turn -0.0 into +0.0 so no real word is */
+/* the sentinel, and a receiver reads words until none is the sentinel.      */
+/* Region = round % 3; the receive step refills another region for reuse.    */
+/* ------------------------------------------------------------------------ */
+void orc_lamport_fill(void* words, int64_t n_words) {
+  for (int64_t i = 0; i < n_words; i++) st32((uint8_t*)words + 4 * i, ORC_LAMPORT_SENTINEL);
+}
+
+void orc_lamport_push(const void* data, int64_t n, void* slot) {
+  for (int64_t i = 0; i < n; i++) {
+    uint16_t v = ld16((const uint8_t*)data + 2 * i);
+    if (v == 0x8000u) v = 0;  /* scrub -0.0 */
+    st16((uint8_t*)slot + 2 * i, v);
+  }
+}
+
+int64_t orc_lamport_reduce_residual_rmsnorm(int W, void* buffer, uint64_t round, int64_t M, int64_t N,
+                                            const void* residual, const void* weight, float eps,
+                                            void* ar, void* residual_out, void* norm_out,
+                                            uint32_t* stale, int64_t cap) {
+  const int64_t n = M * N;
+  uint8_t* base = (uint8_t*)buffer;
+  const int64_t region_bytes = (int64_t)W * n * 2;
+  const uint8_t* region = base + (int64_t)(round % 3) * region_bytes;
+  const void* x[16];
+  for (int r = 0; r < W; r++) x[r] = region + (int64_t)r * n * 2;
+  int64_t n_stale = 0;
+  for (int64_t m = 0; m < M; m++) {
+    /* a row is usable only when no word of it is the sentinel in any rank */
+    int row_ok = 1;
+    for (int r = 0; r < W; r++) {
+      int missing = 0;
+      for (int64_t j = 0; j < N; j += 2) {
+        if (ld32((const uint8_t*)x[r] + 2 * (m * N + j)) == ORC_LAMPORT_SENTINEL) { missing = 1; break; }
+      }
+      if (missing) {
+        if (n_stale < cap) { stale[2 * n_stale] = (uint32_t)r; stale[2 * n_stale + 1] = (uint32_t)m; }
+        n_stale++;
+        row_ok = 0;
+      }
+    }
+    if (!row_ok) {
+      memset((uint8_t*)residual_out + 2 * m * N, 0, (size_t)(2 * N));
+      memset((uint8_t*)norm_out + 2 * m * N, 0, (size_t)(2 * N));
+      if (ar) memset((uint8_t*)ar + 2 * m * N, 0, (size_t)(2 * N));
+      continue;
+    }
+    const void* xr[16];
+    for (int r = 0; r < W; r++) xr[r] = (const uint8_t*)x[r] + 2 * m * N;
+    orc_reduce_residual_rmsnorm(W, xr, (const uint8_t*)residual + 2 * m * N, weight, eps, 1, N, ORC_BF16,
+                                ar ? (uint8_t*)ar + 2 * m * N : 0, (uint8_t*)residual_out + 2 * m * N,
+                                (uint8_t*)norm_out + 2 * m * N, 0);
+  }
+  /* refill the previous round's region so that it can take round + 2 */
+  orc_lamport_fill(base + (int64_t)((round + 2) % 3) * region_bytes, region_bytes / 4);
+  return n_stale;
+}

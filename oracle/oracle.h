@@ -87,6 +87,24 @@ int64_t orc_ll_decode_reduce(int W, const void* const* wires, int64_t data_bytes
                              int dtype, uint32_t expected_flag, void* ar,
                              uint32_t* stale, int64_t cap);
 
+/* ---- Lamport one-shot push (bf16 only): P4 "方案二：Lamport（负零轮询）".
+ *      A receive buffer holds 3 regions x W slots x n bf16 values and starts
+ *      filled with the sentinel word 0x80008000 (two bf16 -0.0).  A push
+ *      writes a rank's values into its slot of region (round % 3) with every
+ *      -0.0 (0x8000) turned into +0.0, so pushed words never equal the
+ *      sentinel.  The receive step treats a sentinel word as "not arrived":
+ *      rows of [M, N] with a missing word in any rank are stale (outputs 0,
+ *      (rank, row) pairs listed, row-major then rank order); other rows get
+ *      the fused rank sum + residual + RMSNorm.  It then refills region
+ *      (round + 2) % 3 -- the previous round's -- with the sentinel. ---- */
+#define ORC_LAMPORT_SENTINEL 0x80008000u
+void    orc_lamport_fill(void* words, int64_t n_words);
+void    orc_lamport_push(const void* data, int64_t n, void* slot);
+int64_t orc_lamport_reduce_residual_rmsnorm(int W, void* buffer, uint64_t round, int64_t M, int64_t N,
+                                            const void* residual, const void* weight, float eps,
+                                            void* ar, void* residual_out, void* norm_out,
+                                            uint32_t* stale, int64_t cap);
+
 #ifdef __cplusplus
 }
 #endif

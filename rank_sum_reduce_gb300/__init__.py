@@ -62,6 +62,12 @@ _SIGS = {
     "car_last_error": (ctypes.c_char_p, []),
     "car_tune_fused": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "car_sync": (ctypes.c_int, [_vp, _vp]),
+    "car_lamport_buffer_bytes": (ctypes.c_size_t, [_vp]),
+    "car_lamport_init": (ctypes.c_int, [_vp, _vp, _vp]),
+    "car_lamport_push": (ctypes.c_int, [_vp, _vp, ctypes.c_int, ctypes.c_uint64, _vp, _vp]),
+    "car_lamport_reduce_residual_rmsnorm": (ctypes.c_int, [_vp, _vp, ctypes.c_uint64, ctypes.c_int, _vp, _vp,
+                                                           ctypes.c_float, _vp, _vp, _vp, _vp]),
+    "car_lamport_report": (ctypes.c_int, [_vp, ctypes.POINTER(car_stale_report)]),
     "car_ll128_decode_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                                        _pvp, ctypes.c_uint64, ctypes.c_int, _vp, _vp,
                                                        ctypes.c_uint32, _vp]),
@@ -160,6 +166,29 @@ def car_ll_decode_reduce(h, wires, expected_flag: int, max_polls: int, ar_out: i
 
 def car_ll_report(h, cap: int = CAR_STALE_LIST_MAX):
     return _report(_lib.car_ll_report, h, cap)
+
+
+def car_lamport_buffer_bytes(h) -> int:
+    return int(_lib.car_lamport_buffer_bytes(h))
+
+
+def car_lamport_init(h, comm: int, stream: int = 0) -> int:
+    return _lib.car_lamport_init(h, comm, stream)
+
+
+def car_lamport_push(h, data: int, rank: int, round_: int, comm: int, stream: int = 0) -> int:
+    return _lib.car_lamport_push(h, data, rank, round_, comm, stream)
+
+
+def car_lamport_reduce_residual_rmsnorm(h, comm: int, round_: int, max_polls: int, residual: int, weight: int,
+                                        eps: float, residual_out: int, norm_out: int, ar_out: int | None,
+                                        stream: int = 0) -> int:
+    return _lib.car_lamport_reduce_residual_rmsnorm(h, comm, round_, max_polls, residual, weight, eps,
+                                                    residual_out, norm_out, ar_out, stream)
+
+
+def car_lamport_report(h, cap: int = CAR_STALE_LIST_MAX):
+    return _report(_lib.car_lamport_report, h, cap)
 
 
 def car_status_string(st: int) -> str:
@@ -271,6 +300,30 @@ class Car:
         st, n, pairs = car_ll_report(self.h, cap)
         if st not in (CAR_OK, CAR_ERR_STALE_FLAG):
             check(st, "car_ll_report")
+        return n, pairs
+
+    @property
+    def lamport_buffer_bytes(self) -> int:
+        return car_lamport_buffer_bytes(self.h)
+
+    def lamport_init(self, comm, stream=None):
+        check(car_lamport_init(self.h, comm.data_ptr(), _stream(stream)), "car_lamport_init")
+
+    def lamport_push(self, data, rank, round_, comm, stream=None):
+        check(car_lamport_push(self.h, data.data_ptr(), rank, round_, comm.data_ptr(), _stream(stream)),
+              "car_lamport_push")
+
+    def lamport_reduce_residual_rmsnorm(self, comm, round_, residual, weight, eps, residual_out, norm_out,
+                                        ar_out=None, max_polls=1, stream=None):
+        check(car_lamport_reduce_residual_rmsnorm(self.h, comm.data_ptr(), round_, max_polls, residual.data_ptr(),
+                                                  weight.data_ptr(), eps, residual_out.data_ptr(),
+                                                  norm_out.data_ptr(), ar_out.data_ptr() if ar_out is not None
+                                                  else None, _stream(stream)), "car_lamport_reduce_residual_rmsnorm")
+
+    def lamport_report(self, cap=CAR_STALE_LIST_MAX):
+        st, n, pairs = car_lamport_report(self.h, cap)
+        if st not in (CAR_OK, CAR_ERR_STALE_FLAG):
+            check(st, "car_lamport_report")
         return n, pairs
 
     def tune_fused(self, kernel=CAR_FUSED_AUTO, cluster=0, threads=0, vpt=0):

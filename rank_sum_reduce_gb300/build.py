@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libcar.so")
 
-SOURCES = ["api.cu", "reduce.cu", "fused.cu", "fused_tma.cu", "ll128.cu", "ll.cu", "ll128_noalloc.cu"]
+SOURCES = ["api.cu", "reduce.cu", "fused.cu", "fused_tma.cu", "ll128.cu", "ll.cu", "ll128_noalloc.cu", "lamport.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                      "-I", INCLUDE, "-I", CSRC]

@@ -53,9 +53,14 @@ struct car_ctx {
   int ll128_encode_grid, ll128_decode_grid;
   int64_t ll_lines;
   int ll_encode_grid, ll_decode_grid;
-  car::StaleLog* log[2];       // [0] LL128, [1] LL (device)
-  cudaStream_t last_stream[2];
-  bool decoded[2];
+  bool lamport_ok;              // bf16 and a row the Lamport receive kernel takes
+  car::FusedShape lamport;
+  int lamport_grid;             // fill / push kernels
+  car::StaleLog* log[3];       // [0] LL128, [1] LL, [2] Lamport (device)
+  cudaStream_t last_stream[3];
+  bool decoded[3];
+  uint64_t calls[3];           // decode calls so far; call c counts in log->n[c & 1]
+  int last_slot[3];
 };
 
 namespace {
@@ -159,6 +164,25 @@ int auto_fused_kernel(const car_ctx* h) {
   return (h->tma_ok && h->M >= (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
 }
 
+// Row-kernel shape for the Lamport receive step: the same rules as the fused
+// row-split kernel, within the Lamport kernel's compiled instances.
+car::FusedShape auto_lamport_shape(int W, int64_t M, int V, int num_sms) {
+  if (M >= 2 * (int64_t)num_sms) {
+    for (int vpt = 1; vpt <= 2; vpt++) {
+      if (!car::lamport_has_variant(W, vpt)) continue;
+      const int t = round_up32((V + vpt - 1) / vpt);
+      if (t <= car::lamport_max_threads(W, vpt)) return car::FusedShape{1, t, vpt, 1};
+    }
+  }
+  int c = 1;
+  if (M < 2 * (int64_t)num_sms) {
+    const int64_t row_input_bytes = (int64_t)(W + 1) * V * 16;
+    while (c < 8 && row_input_bytes / c > 24 * 1024 && (int64_t)c * M < num_sms) c *= 2;
+  }
+  while (c < 8 && (V + c - 1) / c > car::lamport_max_threads(W, 1)) c *= 2;
+  return car::FusedShape{c, std::max(32, round_up32((V + c - 1) / c)), 1, 1};
+}
+
 car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
   int groups = 0;
   cudaError_t e = car::fused_resident_groups(h->dtype, h->W, sh, h->num_sms, &groups);
@@ -168,6 +192,14 @@ car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
   return CAR_OK;
 }
 
+// The log slot of the next decode of this kind (its kernel zeroes the other).
+int next_log_slot(car_ctx* h, int which) {
+  const int slot = (int)(h->calls[which] & 1u);
+  h->calls[which]++;
+  h->last_slot[which] = slot;
+  return slot;
+}
+
 car_status decode_common(car_ctx* h, int which, const void* const* wires, int max_polls,
                          void* ar_out, cudaStream_t s, car::RankPtrs* tbl) {
   car_status st = check_handle(h);
@@ -175,8 +207,6 @@ car_status decode_common(car_ctx* h, int which, const void* const* wires, int ma
   if (max_polls < 1) return CAR_ERR_ARG;
   if ((st = check_table(h, wires, tbl)) != CAR_OK) return st;
   if ((st = check_dev(ar_out)) != CAR_OK) return st;
-  cudaError_t e = cudaMemsetAsync(&h->log[which]->n, 0, sizeof(unsigned long long), s);
-  if (e != cudaSuccess) return cuda_fail(e, "reset stale count");
   h->last_stream[which] = s;
   h->decoded[which] = true;
   return CAR_OK;
@@ -191,7 +221,7 @@ car_status report_common(car_ctx* h, int which, car_stale_report* out) {
   cudaError_t e = cudaStreamSynchronize(h->last_stream[which]);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   unsigned long long n = 0;
-  e = cudaMemcpy(&n, &h->log[which]->n, sizeof(n), cudaMemcpyDeviceToHost);
+  e = cudaMemcpy(&n, &h->log[which]->n[h->last_slot[which]], sizeof(n), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "read stale count");
   const uint64_t listed = std::min<uint64_t>(n, std::min<uint64_t>(out->cap, car::kStaleCap));
   if (listed) {
@@ -303,11 +333,20 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
     h->fused_auto = h->fused;
   }
 
+  h->lamport_ok = h->fused_ok && dtype == CAR_BF16;
+  if (h->lamport_ok) {
+    car::FusedShape sh = auto_lamport_shape(W, M, h->vec_per_row, h->num_sms);
+    int groups = 0;
+    if ((e = car::lamport_resident_groups(W, sh, h->num_sms, &groups)) != cudaSuccess) return fail(e, "lamport occupancy");
+    sh.groups = (int)std::max<int64_t>(1, std::min<int64_t>(M, std::max(groups, 1)));
+    h->lamport = sh;
+    h->lamport_grid = clamp_grid((h->nvec + car::kWireThreads - 1) / car::kWireThreads, 8, h->num_sms);
+  }
   e = cudaMalloc(reinterpret_cast<void**>(&h->d_err), 16);
   if (e != cudaSuccess) return fail(e, "cudaMalloc error word");
   e = cudaMemset(h->d_err, 0, 16);
   if (e != cudaSuccess) return fail(e, "cudaMemset error word");
-  for (int k = 0; k < 2; k++) {
+  for (int k = 0; k < 3; k++) {
     e = cudaMalloc(reinterpret_cast<void**>(&h->log[k]), sizeof(car::StaleLog));
     if (e != cudaSuccess) return fail(e, "cudaMalloc stale log");
     e = cudaMemset(h->log[k], 0, sizeof(unsigned long long) * 2);
@@ -452,7 +491,8 @@ car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_
   car_status st = decode_common(h, 0, wires, max_polls, ar_out, s, &tbl);
   if (st != CAR_OK) return st;
   cudaError_t e = car::launch_ll128_decode_reduce(h->dtype, h->W, tbl, h->D, h->ll128_lines, expected_flag,
-                                                  max_polls, ar_out, h->log[0], h->ll128_decode_grid, s);
+                                                  max_polls, ar_out, h->log[0], next_log_slot(h, 0),
+                                                  h->ll128_decode_grid, s);
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll128_decode_reduce launch");
 }
 
@@ -475,10 +515,69 @@ car_status car_ll_decode_reduce(car_ctx* h, const void* const* wires, uint32_t e
   car_status st = decode_common(h, 1, wires, max_polls, ar_out, s, &tbl);
   if (st != CAR_OK) return st;
   cudaError_t e = car::launch_ll_decode_reduce(h->dtype, h->W, tbl, h->D, expected_flag, max_polls,
-                                               ar_out, h->log[1], h->ll_decode_grid, s);
+                                               ar_out, h->log[1], next_log_slot(h, 1), h->ll_decode_grid, s);
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll_decode_reduce launch");
 }
 
 car_status car_ll_report(car_ctx* h, car_stale_report* out) { return report_common(h, 1, out); }
+
+size_t car_lamport_buffer_bytes(car_ctx* h) {
+  return (live(h) && h->dtype == CAR_BF16) ? (size_t)(3 * (int64_t)h->W * h->D) : 0;
+}
+
+static car_status lamport_checks(car_ctx* h, const void* comm) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if (h->dtype != CAR_BF16) {
+    snprintf(g_err, sizeof(g_err), "the Lamport format packs bf16 pairs: the handle's dtype must be bf16");
+    return CAR_ERR_ARG;
+  }
+  if (!h->lamport_ok) return CAR_ERR_SIZE;
+  return check_dev(comm);
+}
+
+car_status car_lamport_init(car_ctx* h, void* comm, void* stream) {
+  car_status st = lamport_checks(h, comm);
+  if (st != CAR_OK) return st;
+  cudaError_t e = car::launch_lamport_fill(comm, 3 * (int64_t)h->W * h->D, h->lamport_grid,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "lamport fill launch");
+}
+
+car_status car_lamport_push(car_ctx* h, const void* data, int rank, uint64_t round, void* comm, void* stream) {
+  car_status st = lamport_checks(h, comm);
+  if (st != CAR_OK) return st;
+  if (rank < 0 || rank >= h->W) return CAR_ERR_ARG;
+  if ((st = check_dev(data)) != CAR_OK) return st;
+  uint8_t* slot = static_cast<uint8_t*>(comm) + ((int64_t)(round % 3) * h->W + rank) * h->D;
+  cudaError_t e = car::launch_lamport_push(data, h->D, slot, h->lamport_grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "lamport push launch");
+}
+
+car_status car_lamport_reduce_residual_rmsnorm(car_ctx* h, void* comm, uint64_t round, int max_polls,
+                                               const void* residual, const void* weight, float eps,
+                                               void* residual_out, void* norm_out, void* ar_out, void* stream) {
+  car_status st = lamport_checks(h, comm);
+  if (st != CAR_OK) return st;
+  if (max_polls < 1 || !std::isfinite(eps) || eps < 0.f) return CAR_ERR_ARG;
+  if ((st = check_dev(residual)) != CAR_OK) return st;
+  if ((st = check_dev(weight)) != CAR_OK) return st;
+  if ((st = check_dev(residual_out)) != CAR_OK) return st;
+  if ((st = check_dev(norm_out)) != CAR_OK) return st;
+  if (ar_out && !aligned16(ar_out)) return CAR_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->last_stream[2] = s;
+  h->decoded[2] = true;
+  cudaError_t e;
+  const int64_t region_bytes = (int64_t)h->W * h->D;
+  uint8_t* base = static_cast<uint8_t*>(comm);
+  e = car::launch_lamport_reduce(h->W, base + (int64_t)(round % 3) * region_bytes,
+                                 base + (int64_t)((round + 2) % 3) * region_bytes, h->D, residual, weight, eps,
+                                 residual_out, norm_out, ar_out, h->log[2], next_log_slot(h, 2), max_polls, h->M,
+                                 h->N, h->vec_per_row, h->lamport, s);
+  return e == cudaSuccess ? CAR_OK : cuda_fail(e, "lamport receive launch");
+}
+
+car_status car_lamport_report(car_ctx* h, car_stale_report* out) { return report_common(h, 2, out); }
 
 }  // extern "C"

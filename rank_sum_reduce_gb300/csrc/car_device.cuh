@@ -196,20 +196,26 @@ cudaError_t launch_pdl(void (*kernel)(Params...), unsigned grid, unsigned block,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Stale-line record of one decode: a count and the first kStaleCap pairs.
+// Stale-line record of a decode: two counts and the first kStaleCap pairs of
+// the last call.  Call number c counts in n[c & 1] and, once it may touch
+// memory, zeroes n[(c + 1) & 1] for the next call (which waits for this grid
+// before logging), so no separate reset has to be queued between calls.
 constexpr uint32_t kStaleCap = 65536u;  // == CAR_STALE_LIST_MAX
 struct StaleLog {
-  unsigned long long n;
-  unsigned long long reserved;
+  unsigned long long n[2];
   uint32_t entry[kStaleCap][2];
 };
 
-__device__ __forceinline__ void log_stale(StaleLog* log, uint32_t rank, uint32_t line) {
-  const unsigned long long i = atomicAdd(&log->n, 1ull);
+__device__ __forceinline__ void log_stale(StaleLog* log, int slot, uint32_t rank, uint32_t line) {
+  const unsigned long long i = atomicAdd(&log->n[slot], 1ull);
   if (i < kStaleCap) {
     log->entry[i][0] = rank;
     log->entry[i][1] = line;
   }
+}
+
+__device__ __forceinline__ void prepare_next_log(StaleLog* log, int slot) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) log->n[slot ^ 1] = 0ull;
 }
 
 }  // namespace car

@@ -66,7 +66,19 @@ cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t li
                                 void* wire, int grid, cudaStream_t s);
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
-                                       StaleLog* log, int grid, cudaStream_t s);
+                                       StaleLog* log, int log_slot, int grid, cudaStream_t s);
+
+// ---- Lamport one-shot push, bf16 (lamport.cu) ----
+bool lamport_has_variant(int W, int vpt);
+int lamport_max_threads(int W, int vpt);
+cudaError_t lamport_resident_groups(int W, const FusedShape& sh, int num_sms, int* groups);
+cudaError_t launch_lamport_fill(void* words, int64_t bytes, int grid, cudaStream_t s);
+cudaError_t launch_lamport_push(const void* data, int64_t bytes, void* slot, int grid, cudaStream_t s);
+cudaError_t launch_lamport_reduce(int W, const void* region, void* clear_region, int64_t slot_bytes,
+                                  const void* residual, const void* weight, float eps, void* residual_out,
+                                  void* norm_out, void* ar_out, StaleLog* log, int log_slot, int max_polls,
+                                  int64_t rows,
+                                  int64_t cols, int vec_per_row, const FusedShape& sh, cudaStream_t s);
 
 // ---- diagnostics (api.cu): text returned by car_last_error() on this thread ----
 void set_last_error(const char* msg);
@@ -76,7 +88,7 @@ cudaError_t ll_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encod
 cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag, void* wire,
                              int grid, cudaStream_t s);
 cudaError_t launch_ll_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
-                                    uint32_t expected, int max_polls, void* out, StaleLog* log,
+                                    uint32_t expected, int max_polls, void* out, StaleLog* log, int log_slot,
                                     int grid, cudaStream_t s);
 
 }  // namespace car

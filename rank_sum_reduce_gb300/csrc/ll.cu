@@ -33,10 +33,11 @@ template <int DT, int W>
 __global__ void __launch_bounds__(kWireThreads)
     ll_decode_reduce_kernel(const RankPtrs wires, const int nranks, const int64_t lines,
                             const uint32_t expected, const int max_polls, uint2* __restrict__ out,
-                            StaleLog* __restrict__ log) {
+                            StaleLog* __restrict__ log, const int slot) {
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
   pdl_wait_and_release();
+  prepare_next_log(log, slot);
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += step) {
     uint4 raw[R];
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kWireThreads)
     uint2 o = make_uint2(0u, 0u);
     if (bad) {
       for (int r = 0; r < n; r++)
-        if (bad >> r & 1u) log_stale(log, (uint32_t)r, (uint32_t)i);
+        if (bad >> r & 1u) log_stale(log, slot, (uint32_t)r, (uint32_t)i);
     } else {
       // decoded data word of rank r: data1 | data2 << 32 = (raw.x, raw.z)
       uint4 words[R];
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(kWireThreads)
 }
 
 using DecodeFn = void (*)(const RankPtrs, const int, const int64_t, const uint32_t, const int,
-                          uint2*, StaleLog*);
+                          uint2*, StaleLog*, const int);
 
 template <int DT>
 DecodeFn pick_dt(int W) {
@@ -114,10 +115,10 @@ cudaError_t launch_ll_encode(const void* data, int64_t data_bytes, uint32_t flag
 }
 
 cudaError_t launch_ll_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
-                                    uint32_t expected, int max_polls, void* out, StaleLog* log,
+                                    uint32_t expected, int max_polls, void* out, StaleLog* log, int slot,
                                     int grid, cudaStream_t s) {
   return launch_pdl(pick_decode(dtype, W), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes / 8,
-                    expected, max_polls, static_cast<uint2*>(out), log);
+                    expected, max_polls, static_cast<uint2*>(out), log, slot);
 }
 
 }  // namespace car

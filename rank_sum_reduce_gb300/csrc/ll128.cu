@@ -58,7 +58,7 @@ template <int DT, int W>
 __global__ void __launch_bounds__(kWireThreads)
     ll128_decode_reduce_kernel(const RankPtrs wires, const int nranks, const int64_t data_bytes,
                                const int64_t lines, const uint64_t expected, const int max_polls,
-                               uint8_t* __restrict__ out, StaleLog* __restrict__ log) {
+                               uint8_t* __restrict__ out, StaleLog* __restrict__ log, const int slot) {
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
   const int lane = threadIdx.x & 31, c = lane & 15;
@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kWireThreads)
   const int64_t pairs = (lines + 1) / 2;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   pdl_wait_and_release();
+  prepare_next_log(log, slot);
   for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
        wp += nwarps) {
     const int64_t p = 2 * wp + (lane >> 4);
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kWireThreads)
     const uint32_t group_bad = __shfl_sync(kFull, bad, flag_src);
     if (bad) {
       for (int r = 0; r < n; r++)
-        if (bad >> r & 1u) log_stale(log, (uint32_t)r, (uint32_t)line);
+        if (bad >> r & 1u) log_stale(log, slot, (uint32_t)r, (uint32_t)line);
     }
 
     uint4 sum = make_uint4(0u, 0u, 0u, 0u);
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kWireThreads)
 }
 
 using DecodeFn = void (*)(const RankPtrs, const int, const int64_t, const int64_t, const uint64_t,
-                          const int, uint8_t*, StaleLog*);
+                          const int, uint8_t*, StaleLog*, const int);
 
 template <int DT>
 DecodeFn pick_dt(int W) {
@@ -165,9 +166,9 @@ cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t li
 
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
-                                       StaleLog* log, int grid, cudaStream_t s) {
+                                       StaleLog* log, int slot, int grid, cudaStream_t s) {
   return launch_pdl(pick_decode(dtype, W), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes, lines,
-                    expected, max_polls, static_cast<uint8_t*>(out), log);
+                    expected, max_polls, static_cast<uint8_t*>(out), log, slot);
 }
 
 }  // namespace car

@@ -143,9 +143,9 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StaleLog* log = st->log;
-  e = cudaMemsetAsync(&log->n, 0, sizeof(log->n), s);  // the count starts at zero every call
+  e = cudaMemsetAsync(&log->n[0], 0, sizeof(log->n[0]), s);  // the count starts at zero every call
   if (e != cudaSuccess) return cuda_error(e, "clear noalloc stale count");
-  e = launch_ll128_decode_reduce(dtype, W, tbl, D, lines, expected_flag, max_polls, ar_out, log, grid, s);
+  e = launch_ll128_decode_reduce(dtype, W, tbl, D, lines, expected_flag, max_polls, ar_out, log, 0, grid, s);
   if (e != cudaSuccess) return cuda_error(e, "ll128_decode_reduce launch (noalloc)");
   // publish the count and the first `cap` pairs to the caller's buffer
   const size_t bytes = 2 * sizeof(unsigned long long) + (size_t)cap * 2 * sizeof(uint32_t);

@@ -672,3 +672,99 @@ def test_reduce_is_sequential_fp32_adds_in_rank_order(orc, kind):
     for r in range(W - 2, -1, -1):
         rev = (rev + vals[r]).astype(np.float32)
     assert not np.array_equal(rev.view(np.uint32), out.view(np.uint32) if kind == "fp32" else widen(out, kind).view(np.uint32))
+
+
+# ----------------------------------------------------------------------------
+# Lamport one-shot push  (P4 "方案二：Lamport（负零轮询）")
+# ----------------------------------------------------------------------------
+def _lamport_case():
+    (case,) = read_golden("lamport.txt")
+    return case
+
+
+def test_lamport_sentinel_and_scrub_match_the_page(orc):
+    """page value: sentinel 0x80008000, -0.0 scrubbed to +0.0, pair packing."""
+    case = _lamport_case()
+    assert orc.LAMPORT_SENTINEL == int(case["sentinel_hex"], 16)
+    buf = np.zeros(4, dtype=np.uint32)
+    orc.lamport_fill(buf)
+    assert np.all(buf == int(case["sentinel_hex"], 16))
+    pair = np.array([int(h, 16) for h in case["pair_hex"].split()], dtype=np.uint16)
+    W, n = 1, 2
+    comm = np.zeros(3 * W * n, dtype=np.uint16)
+    orc.lamport_push(pair, n, comm, W, 0, 0)
+    assert comm[:2].view(np.uint32)[0] == int(case["word_hex"], 16)
+
+
+def test_lamport_push_never_writes_the_sentinel(orc):
+    """brute force: every bf16 pattern as either half of a word; only -0.0
+    changes (to +0.0), so no pushed word can equal the sentinel."""
+    p = all_patterns16()
+    n = p.size
+    comm = np.zeros(3 * n, dtype=np.uint16)
+    orc.lamport_push(p, n, comm, 1, 0, 0)
+    got = comm[:n]
+    want = p.copy()
+    want[want == 0x8000] = 0
+    assert np.array_equal(got, want)
+    words = np.concatenate([got, got[::-1]]).reshape(-1, 2).copy().view(np.uint32)
+    assert not np.any(words == orc.LAMPORT_SENTINEL)
+
+
+def test_lamport_round_equals_fused_op_on_scrubbed_inputs(orc):
+    """closed form through a pinned function: a complete round gives exactly
+    the fused rank sum + residual + RMSNorm of the scrubbed inputs, reports
+    nothing, and refills the previous round's region with the sentinel while
+    leaving the next one alone."""
+    rng = np.random.default_rng(51)
+    W, M, N = 4, 3, 256
+    xs = [_bf16(rng.standard_normal(M * N)) for _ in range(W)]
+    xs[1][:7] = 0x8000                                     # some -0.0 to scrub
+    res = _bf16(rng.standard_normal(M * N))
+    w = _bf16(rng.uniform(0.5, 1.5, N))
+    comm = np.zeros(3 * W * M * N, dtype=np.uint16)
+    orc.lamport_fill(comm.view(np.uint32))
+    rnd = 4                                                # region 1; refills region 0; region 2 untouched
+    region = lambda k: comm[k * W * M * N:(k + 1) * W * M * N]  # noqa: E731
+    region(0)[:] = 0x1234
+    region(2)[:] = 0x5678
+    for r in range(W):
+        orc.lamport_push(xs[r], M * N, comm, W, r, rnd)
+    ro, no, ar = (np.empty(M * N, dtype=np.uint16) for _ in range(3))
+    n, _ = orc.lamport_reduce_residual_rmsnorm(W, comm, rnd, M, N, res, w, 1e-6, ro, no, ar)
+    assert n == 0
+    scrubbed = [np.where(x == 0x8000, 0, x).astype(np.uint16) for x in xs]
+    ar2, ro2, no2 = (np.empty(M * N, dtype=np.uint16) for _ in range(3))
+    orc.reduce_residual_rmsnorm(scrubbed, res, w, 1e-6, M, N, "bf16", ro2, no2, ar_out=ar2)
+    assert np.array_equal(ar, ar2) and np.array_equal(ro, ro2) and np.array_equal(no, no2)
+    assert np.all(region(0).view(np.uint32) == orc.LAMPORT_SENTINEL)   # (4 + 2) % 3 = 0
+    assert np.all(region(2) == 0x5678)
+
+
+@pytest.mark.parametrize("missing", [(0, 0, 0), (2, 1, 255), (1, 2, 128)])
+def test_lamport_missing_word_makes_its_row_stale(orc, missing):
+    """brute force on small inputs: one word still holding the sentinel makes
+    exactly that (rank, row) stale; the row's outputs are 0; other rows are
+    unaffected."""
+    rng = np.random.default_rng(53)
+    W, M, N = 3, 3, 256
+    xs = [_bf16(rng.standard_normal(M * N)) for _ in range(W)]
+    res = _bf16(rng.standard_normal(M * N))
+    w = _bf16(rng.uniform(0.5, 1.5, N))
+    comm = np.zeros(3 * W * M * N, dtype=np.uint16)
+    orc.lamport_fill(comm.view(np.uint32))
+    for r in range(W):
+        orc.lamport_push(xs[r], M * N, comm, W, r, 0)
+    rank, row, word = missing
+    off = (rank * M * N + row * N + 2 * (word // 2))
+    comm[off:off + 2] = [0x8000, 0x8000]
+    ro, no, ar = (np.full(M * N, 7, dtype=np.uint16) for _ in range(3))
+    n, lst = orc.lamport_reduce_residual_rmsnorm(W, comm, 0, M, N, res, w, 1e-6, ro, no, ar)
+    assert n == 1 and lst.tolist() == [[rank, row]]
+    sl = slice(row * N, (row + 1) * N)
+    assert np.all(ro[sl] == 0) and np.all(no[sl] == 0) and np.all(ar[sl] == 0)
+    keep = np.ones(M * N, dtype=bool)
+    keep[sl] = False
+    ro2, no2, ar2 = (np.empty(M * N, dtype=np.uint16) for _ in range(3))
+    orc.reduce_residual_rmsnorm(xs, res, w, 1e-6, M, N, "bf16", ro2, no2, ar_out=ar2)
+    assert np.array_equal(ro[keep], ro2[keep]) and np.array_equal(no[keep], no2[keep])
