@@ -513,6 +513,62 @@ def ll128_row(arm, iters=10):
             "stale_reported": n_stale, "stale_planted": len(planted), "stale_set_matches": bool(ok)}
 
 
+def ll128_misaligned_row(arm, M, launches, reps=5):
+    """LL128 encode and decode-reduce at W=8, N=8192 bf16 (M rows per rank)
+    with the rank data and the output 16-byte aligned, then both at 4, 8 and
+    12 bytes past a 16-byte boundary (the offsets of "LL128 对齐实验设计"):
+    what the misaligned path costs.  µs per call from graph replay of
+    `launches` calls."""
+    torch, car = arm.torch, arm.car
+    W, N = 8, 8192
+    wl = workloads.custom(W, M, N, "bf16", seed=77)
+    D = wl.data_bytes
+    c = car.Car(W, M, N, "bf16")
+    xs = [workloads.make_x(wl, r, arm.dev) for r in range(W)]
+    wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(W)]
+    keep = []
+
+    def at_offset(src, off):
+        b = torch.empty(D + 32, dtype=torch.uint8, device=arm.dev)
+        keep.append(b)
+        v = b[off:off + D]
+        if src is not None:
+            v.copy_(src.reshape(-1).view(torch.uint8))
+        return v
+
+    def per_call_us(fns):
+        g = capture(torch, fns)
+        us = timed(torch, lambda i: g.replay(), reps) * 1000.0 / len(fns)
+        del g
+        return us
+
+    row = {"workload": f"ll128_w8_m{M}_n8192_bf16", "bytes_per_rank": D}
+    outs = {}
+    offsets = (("aligned", 0), ("offset4", 4), ("offset8", 8), ("offset12", 12))
+    for name, off in offsets:
+        data = [at_offset(x, off) for x in xs]
+        out = at_offset(None, off)
+        enc = [(lambda d, wv: (lambda s: c.ll128_encode(d, 7, wv, stream=s)))(data[i % W], wires[i % W])
+               for i in range(launches)]
+        dec = [lambda s: c.ll128_decode_reduce(wires, 7, out, stream=s)] * launches
+        e_us = per_call_us(enc)
+        d_us = per_call_us(dec)
+        torch.cuda.synchronize()
+        outs[name] = out.clone()
+        row[name] = {"encode_us": round(e_us, 3), "encode_GBps": round((D + ll128_wire_bytes(D)) / e_us / 1e3, 1),
+                     "decode_reduce_us": round(d_us, 3),
+                     "decode_reduce_GBps": round((W * ll128_wire_bytes(D) + D) / d_us / 1e3, 1)}
+    row["misaligned_over_aligned"] = {
+        name: {k: round(row[name][k] / row["aligned"][k], 3) for k in ("encode_us", "decode_reduce_us")}
+        for name, _ in offsets[1:]}
+    row["outputs_equal"] = all(bool(torch.equal(outs["aligned"], outs[name])) for name, _ in offsets[1:])
+    row["stale_reported"] = c.ll128_report()[0]
+    row["l2"] = "warm (wires fit in L2)" if W * ll128_wire_bytes(D) < L2_BYTES else "cold (wires exceed L2)"
+    c.close()
+    del wires, xs, keep
+    return row
+
+
 def ll_row(arm, iters=20):
     """LL encode + validate/decode/reduce at the headline shape (W=8, 8 MB per rank)."""
     torch, car = arm.torch, arm.car
@@ -670,6 +726,8 @@ def main():
         rows["two_shot_m512_w8"] = two_shot_row(arm)
         rows["ll128_w16_decode_reduce"] = ll128_row(arm)
         rows["ll_m512_w8"] = ll_row(arm)
+        rows["ll128_misaligned_1MiB"] = ll128_misaligned_row(arm, 64, 256)
+        rows["ll128_misaligned_64MiB"] = ll128_misaligned_row(arm, 4096, 16)
         torch.cuda.empty_cache()
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None

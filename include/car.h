@@ -51,7 +51,7 @@ typedef enum { CAR_BF16 = 0, CAR_FP16 = 1, CAR_FP32 = 2 } car_dtype;
 typedef enum {
   CAR_OK = 0,
   CAR_ERR_ARG = 1,        /* NULL pointer, W/M/N/dtype out of range, bad max_polls */
-  CAR_ERR_ALIGN = 2,      /* a device pointer not 16-byte aligned                   */
+  CAR_ERR_ALIGN = 2,      /* a device pointer below the alignment its call needs    */
   CAR_ERR_SIZE = 3,       /* N*s not a multiple of 16, size overflow, row too long  */
   CAR_ERR_CUDA = 4,       /* CUDA runtime error (see car_last_error)                */
   CAR_ERR_STALE_FLAG = 5, /* a decode found lines whose flag was not the expected one */
@@ -161,11 +161,17 @@ size_t car_ll128_wire_bytes(car_ctx* h);
 /* Encode one rank's D data bytes into LL128 lines: line k holds data words
  * 15k..15k+14 (uint64, little-endian, zero past the end of the data) in
  * words 0..14 and `flag` in word 15.
- *   data : dev, D bytes.   wire : dev, car_ll128_wire_bytes(h) bytes.
+ *   data : dev, D bytes, aligned to the element size only: a buffer at a
+ *          2..14-byte offset from a 16-byte boundary is read with aligned
+ *          16-byte loads of the blocks that hold it and realigned in registers
+ *          (P2 "LL128 对齐为何重要" measures NCCL's misaligned path).
+ *   wire : dev, car_ll128_wire_bytes(h) bytes, 16-byte aligned.
  * Errors: CAR_ERR_HANDLE, CAR_ERR_ARG, CAR_ERR_ALIGN, CAR_ERR_CUDA. */
 car_status car_ll128_encode(car_ctx* h, const void* data, uint64_t flag, void* wire, void* stream);
 
-/* Validate, decode and reduce W LL128 wires: line k of rank r is valid when
+/* Validate, decode and reduce W LL128 wires (ar_out, like the encode's data,
+ * needs only element alignment; no byte outside ar_out[0, D) is written):
+ * line k of rank r is valid when
  * its word 15 equals expected_flag.  A line found stale is checked again up
  * to max_polls - 1 more times (re-reading the whole line each time); there
  * is no unbounded wait.  For every line valid in all ranks, each element of
@@ -208,7 +214,8 @@ car_status car_ll128_report(car_ctx* h, car_stale_report* out);
  *
  * Arguments: the shape (W, M, N, dtype) and data as for car_create and
  * car_ll128_decode_reduce (wires: W dev pointers of 128*ceil(M*N*s/120)
- * bytes; ar_out: dev, M*N*s bytes).  stale_out: dev, 16-byte aligned,
+ * bytes, 16-byte aligned; ar_out: dev, M*N*s bytes, element-aligned).
+ * stale_out: dev, 16-byte aligned,
  * 16 + 8*cap bytes; after the call completes on `stream` it holds the
  * uint64 count of stale (rank, line) pairs at byte 0, 8 reserved bytes, then
  * min(count, cap) pairs of uint32 (rank, line) (bytes past those are

@@ -112,6 +112,12 @@ car_status check_dev(const void* p) {
   return aligned16(p) ? CAR_OK : CAR_ERR_ALIGN;
 }
 
+// Rank data of the LL128 calls needs only element alignment.
+car_status check_dev_elem(const void* p, int es) {
+  if (!p) return CAR_ERR_ARG;
+  return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)es) == 0 ? CAR_OK : CAR_ERR_ALIGN;
+}
+
 int clamp_grid(int64_t needed, int per_sm, int num_sms) {
   const int64_t cap = (int64_t)std::max(per_sm, 1) * num_sms;
   return (int)std::max<int64_t>(1, std::min(needed, cap));
@@ -206,7 +212,8 @@ car_status decode_common(car_ctx* h, int which, const void* const* wires, int ma
   if (st != CAR_OK) return st;
   if (max_polls < 1) return CAR_ERR_ARG;
   if ((st = check_table(h, wires, tbl)) != CAR_OK) return st;
-  if ((st = check_dev(ar_out)) != CAR_OK) return st;
+  // LL128 output may sit at any element offset; LL output stays 16-byte aligned
+  if ((st = which == 0 ? check_dev_elem(ar_out, h->es) : check_dev(ar_out)) != CAR_OK) return st;
   h->last_stream[which] = s;
   h->decoded[which] = true;
   return CAR_OK;
@@ -477,7 +484,7 @@ size_t car_ll_wire_bytes(car_ctx* h) { return live(h) ? (size_t)(16 * h->ll_line
 car_status car_ll128_encode(car_ctx* h, const void* data, uint64_t flag, void* wire, void* stream) {
   car_status st = check_handle(h);
   if (st != CAR_OK) return st;
-  if ((st = check_dev(data)) != CAR_OK) return st;
+  if ((st = check_dev_elem(data, h->es)) != CAR_OK) return st;
   if ((st = check_dev(wire)) != CAR_OK) return st;
   cudaError_t e = car::launch_ll128_encode(data, h->D, h->ll128_lines, flag, wire, h->ll128_encode_grid,
                                            static_cast<cudaStream_t>(stream));

@@ -23,12 +23,45 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// Bytes [s, s + 16) of the 32-byte concatenation (a, b), for 0 <= s < 16:
+// word selection by s / 4, then a funnel shift by the remaining bytes.
+__device__ __forceinline__ uint32_t pick4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, int q) {
+  return q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
+}
+__device__ __forceinline__ uint4 bytes_at(uint4 a, uint4 b, int s) {
+  const int q = s >> 2;
+  const uint32_t sh = (uint32_t)(s & 3) * 8u;
+  const uint32_t w0 = pick4(a.x, a.y, a.z, a.w, q);
+  const uint32_t w1 = pick4(a.y, a.z, a.w, b.x, q);
+  const uint32_t w2 = pick4(a.z, a.w, b.x, b.y, q);
+  const uint32_t w3 = pick4(a.w, b.x, b.y, b.z, q);
+  const uint32_t w4 = pick4(b.x, b.y, b.z, b.w, q);
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh), __funnelshift_r(w2, w3, sh),
+                    __funnelshift_r(w3, w4, sh));
+}
+__device__ __forceinline__ uint4 shfl_down16(uint4 v, int by, int width) {
+  return make_uint4(__shfl_down_sync(0xFFFFFFFFu, v.x, by, width), __shfl_down_sync(0xFFFFFFFFu, v.y, by, width),
+                    __shfl_down_sync(0xFFFFFFFFu, v.z, by, width), __shfl_down_sync(0xFFFFFFFFu, v.w, by, width));
+}
+__device__ __forceinline__ uint4 shfl_idx16(uint4 v, int src) {
+  return make_uint4(__shfl_sync(0xFFFFFFFFu, v.x, src), __shfl_sync(0xFFFFFFFFu, v.y, src),
+                    __shfl_sync(0xFFFFFFFFu, v.z, src), __shfl_sync(0xFFFFFFFFu, v.w, src));
+}
+
 // Lane c of a half-warp holds data vector c (c < 15) of the line pair.  Wire
 // chunk c of the pair is:
 //   c <= 6      : data words 2c, 2c+1          -> (x_c, y_c)
 //   c == 7      : data word 14, flag            -> (x_7, flag)
 //   8 <= c < 15 : data words 2c-1, 2c           -> (y_{c-1}, x_c)
 //   c == 15     : data word 29, flag            -> (y_14, flag)
+//
+// Misaligned data (kMis: the data pointer is element- but not 16-byte
+// aligned; P2 "LL128 对齐为何重要" stages such buffers through shared memory):
+// lane c loads the aligned 16-byte block c of the pair's range -- every block
+// that holds a data byte lies in the same page as that byte, so the load is
+// safe -- and rebuilds data vector c from blocks c and c + 1 (one lane
+// shuffle and a funnel shift), staying in registers.
+template <bool kMis>
 __global__ void __launch_bounds__(kWireThreads)
     ll128_encode_kernel(const uint8_t* __restrict__ data, const int64_t data_bytes,
                         const int64_t lines, const uint64_t flag, uint8_t* __restrict__ wire) {
@@ -41,7 +74,15 @@ __global__ void __launch_bounds__(kWireThreads)
     const int64_t p = 2 * wp + (lane >> 4);
     uint4 d = make_uint4(0u, 0u, 0u, 0u);
     const int64_t doff = p * 240 + 16 * c;
-    if (p < pairs && c < 15 && doff < data_bytes) d = ld_stream(data + doff);
+    if (!kMis) {
+      if (p < pairs && c < 15 && doff < data_bytes) d = ld_stream(data + doff);
+    } else {
+      const int m = (int)(reinterpret_cast<uintptr_t>(data) & 15u);
+      uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+      if (p < pairs && doff - m < data_bytes) blk = ld_stream(data - m + doff);
+      const uint4 nxt = shfl_down16(blk, 1, 16);
+      if (p < pairs && c < 15 && doff < data_bytes) d = bytes_at(blk, nxt, m);
+    }
     const uint64_t x = lo64(d), y = hi64(d);
     const uint64_t y_prev = __shfl_up_sync(kFull, y, 1, 16);
     const uint64_t first = c <= 7 ? x : y_prev;
@@ -54,7 +95,13 @@ __global__ void __launch_bounds__(kWireThreads)
 // Inverse mapping: output vector o (o < 15) of the pair is
 //   o <= 6 : (x_o, y_o);  o == 7 : (x_7, x_8);  o >= 8 : (y_o, x_{o+1})
 // where (x_c, y_c) is wire chunk c after the rank sum.
-template <int DT, int W>
+//
+// Misaligned output (kMisOut): a warp owns the 480 data bytes of its two
+// pairs.  Lane b builds aligned output block b (0..30) from data vectors b-1
+// and b; the blocks inside the warp's range are stored whole, the first and
+// last (shared with the neighbouring warps) and any block past the end of the
+// data are stored 2 bytes at a time, only over the bytes this warp owns.
+template <int DT, int W, bool kMisOut>
 __global__ void __launch_bounds__(kWireThreads)
     ll128_decode_reduce_kernel(const RankPtrs wires, const int nranks, const int64_t data_bytes,
                                const int64_t lines, const uint64_t expected, const int max_polls,
@@ -122,29 +169,58 @@ __global__ void __launch_bounds__(kWireThreads)
     const uint64_t first = c <= 7 ? x : y;
     const uint64_t second = c <= 6 ? y : x_next;
     const int64_t ooff = p * 240 + 16 * c;
-    if (p < pairs && c < 15 && ooff < data_bytes) st16(out + ooff, make16(first, second));
+    if (!kMisOut) {
+      if (p < pairs && c < 15 && ooff < data_bytes) st16(out + ooff, make16(first, second));
+    } else {
+      // data vector d (0..29) of the warp sits in lane d (d < 15) or d + 1
+      const int m = (int)(reinterpret_cast<uintptr_t>(out) & 15u);
+      const uint4 dv = make16(first, second);
+      const int b = lane;
+      const int prev = b == 0 ? 0 : (b - 1 < 15 ? b - 1 : b);
+      const int cur = b < 15 ? b : (b < 31 ? b + 1 : 31);
+      const uint4 va = shfl_idx16(dv, prev);
+      const uint4 vb = shfl_idx16(dv, cur);
+      const uint4 blk = bytes_at(va, vb, 16 - m);
+      const int64_t wbase = 480 * wp;
+      const int64_t dw = data_bytes - wbase < 480 ? data_bytes - wbase : 480;
+      const int lo = m - 16 * b > 0 ? m - 16 * b : 0;
+      const int64_t hi64v = dw - 16 * b + m;
+      const int hi = hi64v < 16 ? (int)hi64v : 16;
+      uint8_t* dst = out - m + wbase + 16 * b;
+      if (b < 31 && lo < hi) {
+        if (lo == 0 && hi == 16) {
+          st16(dst, blk);
+        } else {
+          const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            if (2 * i >= lo && 2 * i < hi)
+              *reinterpret_cast<uint16_t*>(dst + 2 * i) = (uint16_t)(w4[i >> 1] >> (16 * (i & 1)));
+        }
+      }
+    }
   }
 }
 
 using DecodeFn = void (*)(const RankPtrs, const int, const int64_t, const int64_t, const uint64_t,
                           const int, uint8_t*, StaleLog*, const int);
 
-template <int DT>
+template <int DT, bool kMis>
 DecodeFn pick_dt(int W) {
   switch (W) {
-    case 2: return ll128_decode_reduce_kernel<DT, 2>;
-    case 4: return ll128_decode_reduce_kernel<DT, 4>;
-    case 8: return ll128_decode_reduce_kernel<DT, 8>;
-    case 16: return ll128_decode_reduce_kernel<DT, 16>;
-    default: return ll128_decode_reduce_kernel<DT, 0>;
+    case 2: return ll128_decode_reduce_kernel<DT, 2, kMis>;
+    case 4: return ll128_decode_reduce_kernel<DT, 4, kMis>;
+    case 8: return ll128_decode_reduce_kernel<DT, 8, kMis>;
+    case 16: return ll128_decode_reduce_kernel<DT, 16, kMis>;
+    default: return ll128_decode_reduce_kernel<DT, 0, kMis>;
   }
 }
 
-DecodeFn pick_decode(int dtype, int W) {
+DecodeFn pick_decode(int dtype, int W, bool mis = false) {
   switch (dtype) {
-    case kBF16: return pick_dt<kBF16>(W);
-    case kFP16: return pick_dt<kFP16>(W);
-    default: return pick_dt<kFP32>(W);
+    case kBF16: return mis ? pick_dt<kBF16, true>(W) : pick_dt<kBF16, false>(W);
+    case kFP16: return mis ? pick_dt<kFP16, true>(W) : pick_dt<kFP16, false>(W);
+    default: return mis ? pick_dt<kFP32, true>(W) : pick_dt<kFP32, false>(W);
   }
 }
 
@@ -155,19 +231,21 @@ cudaError_t ll128_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* en
       decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W)), kWireThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      encode_blocks_per_sm, reinterpret_cast<const void*>(ll128_encode_kernel), kWireThreads, 0);
+      encode_blocks_per_sm, reinterpret_cast<const void*>(ll128_encode_kernel<false>), kWireThreads, 0);
 }
 
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
                                 void* wire, int grid, cudaStream_t s) {
-  return launch_pdl(ll128_encode_kernel, (unsigned)grid, kWireThreads, 0, s, 1, static_cast<const uint8_t*>(data),
-                    data_bytes, lines, flag, static_cast<uint8_t*>(wire));
+  const bool mis = (reinterpret_cast<uintptr_t>(data) & 15u) != 0;
+  return launch_pdl(mis ? ll128_encode_kernel<true> : ll128_encode_kernel<false>, (unsigned)grid, kWireThreads, 0,
+                    s, 1, static_cast<const uint8_t*>(data), data_bytes, lines, flag, static_cast<uint8_t*>(wire));
 }
 
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
                                        StaleLog* log, int slot, int grid, cudaStream_t s) {
-  return launch_pdl(pick_decode(dtype, W), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes, lines,
+  const bool mis = (reinterpret_cast<uintptr_t>(out) & 15u) != 0;
+  return launch_pdl(pick_decode(dtype, W, mis), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes, lines,
                     expected, max_polls, static_cast<uint8_t*>(out), log, slot);
 }
 

@@ -115,7 +115,7 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
     if (reinterpret_cast<uintptr_t>(wires[r]) & 15u) return CAR_ERR_ALIGN;
     tbl.p[r] = wires[r];
   }
-  if ((reinterpret_cast<uintptr_t>(ar_out) & 15u) || (reinterpret_cast<uintptr_t>(stale_out) & 15u))
+  if ((reinterpret_cast<uintptr_t>(ar_out) % (uintptr_t)es) || (reinterpret_cast<uintptr_t>(stale_out) & 15u))
     return CAR_ERR_ALIGN;
 
   int dev = -1;
