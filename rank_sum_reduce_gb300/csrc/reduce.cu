@@ -10,7 +10,11 @@
 // and capped at the resident CTA count of the 152 SMs (no 36-block cap), every
 // thread keeps U x W independent 16-byte loads in flight, and the rank inputs
 // come from local HBM instead of NVLink peers, so there is no entry or exit
-// barrier.  Roofline: HBM, (W + 1) * 16 bytes per vector.
+// barrier.  Each CTA takes one contiguous, equal share of the vectors (within
+// one), so all CTAs finish together; a grid-stride loop over fixed waves of
+// grid * threads * U vectors leaves part of the grid idle in the last wave
+// (8 MB per rank at W = 8 is 3.37 waves).  Roofline: HBM, (W + 1) * 16 bytes
+// per vector.
 #include "car_device.cuh"
 #include "car_launch.h"
 
@@ -24,14 +28,16 @@ __global__ void __launch_bounds__(kReduceThreads)
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
   pdl_wait_and_release();
-  const int64_t step = (int64_t)gridDim.x * kReduceThreads * U;
-  for (int64_t base = (int64_t)blockIdx.x * kReduceThreads * U + threadIdx.x; base < nvec;
-       base += step) {
+  // this CTA's share [lo, hi): nvec / grid vectors, one more for the first nvec % grid CTAs
+  const int64_t share = nvec / gridDim.x, extra = nvec % gridDim.x;
+  const int64_t lo = share * blockIdx.x + (blockIdx.x < extra ? blockIdx.x : extra);
+  const int64_t hi = lo + share + (blockIdx.x < extra ? 1 : 0);
+  for (int64_t base = lo + threadIdx.x; base < hi; base += kReduceThreads * U) {
     uint4 raw[U][R];
 #pragma unroll
     for (int u = 0; u < U; u++) {
       const int64_t v = base + (int64_t)u * kReduceThreads;
-      if (v < nvec) {
+      if (v < hi) {
 #pragma unroll
         for (int r = 0; r < R; r++)
           if (r < n) raw[u][r] = ld_stream(static_cast<const uint4*>(in.p[r]) + v);
@@ -40,7 +46,7 @@ __global__ void __launch_bounds__(kReduceThreads)
 #pragma unroll
     for (int u = 0; u < U; u++) {
       const int64_t v = base + (int64_t)u * kReduceThreads;
-      if (v < nvec) {
+      if (v < hi) {
         float acc[Pack<DT>::kN];
         rank_sum<DT, R>(raw[u], n, acc);
         st16(out + v, Pack<DT>::narrow(acc));
