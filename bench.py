@@ -389,10 +389,33 @@ def latency_row(arm, wl, outputs, calls=12000):
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / (reps * n)
-    c.close()
     del g
+    # the same calls launched one by one on a stream through the C ABI (no
+    # graph): device time per call, and host wall time spent in each call
+    cs = torch.cuda.current_stream()
+    plain = min(n, 2000)
+
+    def issue():
+        for S, tbl in zip(sets[:plain], tables[:plain]):
+            st = lib.car_reduce_residual_rmsnorm(h, tbl, S["res"].data_ptr(), S["w"].data_ptr(), eps,
+                                                 S["ro"].data_ptr(), S["no"].data_ptr(),
+                                                 S["ar"].data_ptr() if outputs == 3 else None, cs.cuda_stream)
+            if st:
+                raise RuntimeError(car.car_last_error())
+    issue()
+    torch.cuda.synchronize()
+    e0.record(cs)
+    t0 = time.perf_counter()
+    issue()
+    t1 = time.perf_counter()
+    e1.record(cs)
+    torch.cuda.synchronize()
+    stream_us = e0.elapsed_time(e1) * 1000.0 / plain
+    host_us = (t1 - t0) * 1e6 / plain
+    c.close()
     return {"us_per_call": round(us, 3), "calls_per_graph": n, "bytes_per_call": set_bytes,
             "GBps": round(set_bytes / (us * 1e-6) / 1e9, 1),
+            "stream_launch_us_per_call": round(stream_us, 3), "host_us_per_call": round(host_us, 3),
             "l2": "cold (sets exceed 2x L2)" if n * set_bytes > 2 * L2_BYTES else "partly warm"}
 
 
