@@ -35,6 +35,9 @@ if ROOT not in sys.path:
 
 import workloads  # noqa: E402
 
+# steps of the end-to-end measurement run on this many streams in turn, so
+# one step's host copies overlap the next step's
+E2E_STREAMS = 3
 HEADLINE = "m512_w8"
 METRIC = "HBM GB/s (fraction of GB300 peak) for W-way reduce+RMSNorm; µs/call at M=1"
 FALLBACK_HBM_GBS = 6800.0
@@ -311,43 +314,58 @@ def headline(arm, wl, steps, warmup, rank, world):
             "t0": t0, "t1": t1, "launches": 2 * steps}
 
 
-def e2e(arm, wl, steps, warmup):
+def e2e(arm, wl, steps, warmup, streams=1):
     """Same step through the public API with pinned host buffers: H2D of the
-    step's inputs, the two calls, D2H of its three outputs, all timed."""
+    step's inputs, the two calls, D2H of its three outputs, all timed.  With
+    streams > 1, step i runs on stream i % streams with that stream's own
+    device and host buffers, so one step's copies overlap the neighbouring
+    steps' copies and kernels (the copy engines work in both directions at
+    once); every step still copies all of its inputs in and outputs out."""
     torch, car = arm.torch, arm.car
     dev = arm.dev
     xs, res, w = workloads.make_inputs(wl, dev)
     hx = [x.cpu().pin_memory() for x in xs]
     hres, hw = res.cpu().pin_memory(), w.cpu().pin_memory()
-    dx = [torch.empty_like(x) for x in xs]
-    dres, dw = torch.empty_like(res), torch.empty_like(w)
-    outs = [torch.empty_like(res) for _ in range(3)]
-    houts = [torch.empty_like(hres).pin_memory() for _ in range(3)]
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
+    lanes = []
+    for _ in range(streams):
+        lanes.append({"stream": torch.cuda.Stream() if streams > 1 else torch.cuda.current_stream(),
+                      "dx": [torch.empty_like(x) for x in xs], "dres": torch.empty_like(res),
+                      "dw": torch.empty_like(w), "outs": [torch.empty_like(res) for _ in range(3)],
+                      "houts": [torch.empty_like(hres).pin_memory() for _ in range(3)]})
 
-    def step():
-        for d, hsrc in zip(dx, hx):
-            d.copy_(hsrc, non_blocking=True)
-        dres.copy_(hres, non_blocking=True)
-        dw.copy_(hw, non_blocking=True)
-        c.reduce(dx, outs[0])
-        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, outs[1], outs[2])
-        for ho, o in zip(houts, outs):
-            ho.copy_(o, non_blocking=True)
+    def step(i):
+        L = lanes[i % streams]
+        with torch.cuda.stream(L["stream"]):
+            for d, hsrc in zip(L["dx"], hx):
+                d.copy_(hsrc, non_blocking=True)
+            L["dres"].copy_(hres, non_blocking=True)
+            L["dw"].copy_(hw, non_blocking=True)
+            c.reduce(L["dx"], L["outs"][0])
+            c.reduce_residual_rmsnorm(L["dx"], L["dres"], L["dw"], wl.eps, L["outs"][1], L["outs"][2])
+            for ho, o in zip(L["houts"], L["outs"]):
+                ho.copy_(o, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    e0.record(main)
+    for L in lanes:
+        if L["stream"] is not main:
+            L["stream"].wait_event(e0)
+    for i in range(steps):
+        step(i)
+    for L in lanes:
+        if L["stream"] is not main:
+            main.wait_stream(L["stream"])
+    e1.record(main)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     c.close()
     h2d = sum(x.numel() * x.element_size() for x in hx) + hres.numel() * hres.element_size() + hw.numel() * hw.element_size()
-    d2h = sum(o.numel() * o.element_size() for o in houts)
+    d2h = sum(o.numel() * o.element_size() for o in lanes[0]["houts"])
     return ms, h2d, d2h
 
 
@@ -765,9 +783,11 @@ def main():
     ms_per_step, value = aggregate(H["region_ms"], args.steps, step_bytes, world)
 
     e2e_steps = max(3, min(args.steps, 50))
-    e2e_ms, h2d, d2h = e2e(arm, wl, e2e_steps, 3)
+    e2e_ms, h2d, d2h = e2e(arm, wl, e2e_steps, 3, streams=E2E_STREAMS)
     e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_gbps = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_serial_ms, _, _ = e2e(arm, wl, e2e_steps, 3, streams=1)
+    e2e_serial_ms = max_over_ranks(e2e_serial_ms, world)
 
     if rank != 0:
         if world > 1:
@@ -813,7 +833,9 @@ def main():
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "traffic_note": traffic_note},
         "e2e": {"value": round(e2e_gbps, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "streams": E2E_STREAMS,
+                "serial_value": round(world * step_bytes / (e2e_serial_ms * 1e-3) / 1e9, 2),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "clocks": clocks,
         "cpu_baseline": cpu,
         "rows": rows,
