@@ -44,6 +44,7 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
 // ---- fused, many rows: TMA bulk copies into a shared-memory ring (fused_tma.cu) ----
 struct FusedTmaShape {
   int cluster;    // CTAs sharing each row (1 or 2)
+  int ls;         // trailing slices of a row loaded by the consumers, not bulk-copied (0 or 3)
   int consumers;  // consumer threads (the CTA adds one producer warp)
   int vpt;        // 16-byte vectors per consumer thread (1, 2, 4, 8)
   int slots;      // ring depth in row slices

@@ -28,6 +28,8 @@ namespace car {
 namespace {
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+// Slices per row loaded by the consumers instead of bulk copies (see run_consumers).
+constexpr int kRegSlices = 3;
 
 struct TmaParams {
   RankPtrs in;
@@ -43,6 +45,7 @@ struct TmaParams {
   int row_bytes;       // N * s
   int vec_per_row;
   int slots;           // ring depth
+  int tma_slices;      // leading slices of a row that come by bulk copy (the rest by plain loads)
   int consumers;       // consumer threads (multiple of 32)
   int nranks;
   int cluster;         // CTAs sharing a row (1 or 2): each takes 1/cluster of the columns
@@ -168,7 +171,7 @@ __device__ __forceinline__ void run_producer(const TmaParams& p, uint8_t* ring, 
   bool ok = true;
   for (int64_t row = group; row < p.rows && ok; row += ngroups) {
     const int64_t off = row * (int64_t)p.row_bytes + (int64_t)crank * slice;
-    for (int q = 0; q <= n; q++) {
+    for (int q = 0; q < p.tma_slices; q++) {
       // slot reuse: wait until every consumer warp released its previous fill
       if (issued >= (uint64_t)S && !wait_bounded(&empty[slot], phase ^ 1u, s_abort)) {
         ok = false;
@@ -204,7 +207,15 @@ __device__ __forceinline__ void run_producer(const TmaParams& p, uint8_t* ring, 
 // Consumers: fold each rank slice as it lands, add the residual, store ar and
 // residual_out, combine the row's sum of squares (CTA, then cluster), store
 // norm_out.  On a failed wait they record it and leave the row loop.
-template <int DT, int W, int VPT>
+//
+// With LS > 0 the last LS slices of a row (the last ranks and the residual)
+// skip the ring: each consumer loads its own columns of them with 16-byte
+// loads issued when the row starts, and folds them, still in rank order,
+// after the bulk-copied slices.  One thread issues the bulk copies one after
+// another (about 0.32 us each for 16 KB on GB300), so fewer copies per row
+// shorten every row whose SM is not waiting on HBM anyway: the first row
+// and the last, partial wave.
+template <int DT, int W, int VPT, int LS>
 __device__ __forceinline__ void run_consumers(const TmaParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty,
                                               uint64_t* rowbar, uint64_t* xbar, float* s_warp, float* s_part,
                                               float* s_total, volatile int* s_abort, int S, int slice, int cols,
@@ -226,11 +237,23 @@ __device__ __forceinline__ void run_consumers(const TmaParams& p, uint8_t* ring,
   int slot = 0;
   uint32_t phase = 0, it = 0;
   bool failed = false;
+  const int nt = n + 1 - LS;  // slices that come through the ring
   for (int64_t row = group; row < p.rows && !failed; row += ngroups, it++) {
     const int64_t rbase = row * (int64_t)p.vec_per_row + col0;
     float acc[VPT][E];
     float ss = 0.f;
-    for (int q = 0; q <= n; q++) {
+    uint4 lreg[LS > 0 ? LS : 1][VPT];
+    if constexpr (LS > 0) {
+#pragma unroll
+      for (int j = 0; j < LS; j++) {
+        const int q = nt + j;
+        const uint4* src = q < n ? static_cast<const uint4*>(p.in.p[q]) : reinterpret_cast<const uint4*>(p.residual);
+#pragma unroll
+        for (int k = 0; k < VPT; k++)
+          if (ok_col[k]) lreg[j][k] = ld_stream(src + rbase + threadIdx.x + k * T);
+      }
+    }
+    for (int q = 0; q < nt; q++) {
       if (!wait_bounded(&full[slot], phase, s_abort)) {
         failed = true;
         break;
@@ -273,6 +296,32 @@ __device__ __forceinline__ void run_consumers(const TmaParams& p, uint8_t* ring,
       }
     }
     if (failed) break;
+    if constexpr (LS > 0) {
+#pragma unroll
+      for (int j = 0; j < LS; j++) {
+        const int q = nt + j;
+#pragma unroll
+        for (int k = 0; k < VPT; k++) {
+          if (ok_col[k]) {
+            const int v = threadIdx.x + k * T;
+            float t[E];
+            Pack<DT>::widen(lreg[j][k], t);
+            if (q < n) {
+#pragma unroll
+              for (int e = 0; e < E; e++) acc[k][e] = q == 0 ? t[e] : __fadd_rn(acc[k][e], t[e]);
+            } else {
+              if (p.ar_out) st16(p.ar_out + rbase + v, Pack<DT>::narrow(acc[k]));
+#pragma unroll
+              for (int e = 0; e < E; e++) {
+                acc[k][e] = __fadd_rn(acc[k][e], t[e]);  // acc now holds h
+                ss = fmaf(acc[k][e], acc[k][e], ss);
+              }
+              st16(p.residual_out + rbase + v, Pack<DT>::narrow(acc[k]));
+            }
+          }
+        }
+      }
+    }
     // row statistic: warp partials -> CTA partial -> (cluster) row total
     ss = warp_sum(ss);
     if (lane == 0) {
@@ -332,7 +381,7 @@ __device__ __forceinline__ void run_consumers(const TmaParams& p, uint8_t* ring,
   }
 }
 
-template <int DT, int W, int VPT>
+template <int DT, int W, int VPT, int LS>
 __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(const TmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int S = p.slots;
@@ -373,8 +422,8 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
   if (warp == nconsumer_warps) {
     if (lane == 0) run_producer(p, ring, full, empty, s_abort, S, slice, n, crank, group, ngroups);
   } else {
-    run_consumers<DT, W, VPT>(p, ring, full, empty, rowbar, xbar, s_warp, s_part, s_total, s_abort, S, slice,
-                              cols, n, crank, group, ngroups, nconsumer_warps);
+    run_consumers<DT, W, VPT, LS>(p, ring, full, empty, rowbar, xbar, s_warp, s_part, s_total, s_abort, S, slice,
+                                  cols, n, crank, group, ngroups, nconsumer_warps);
   }
   // A CTA leaves only when its cluster peer is done with its shared memory
   // (every wait above is bounded, so every thread gets here).
@@ -384,14 +433,18 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
 using TmaFn = void (*)(const TmaParams);
 
 template <int DT>
-TmaFn pick_dt(int W, int vpt) {
-#define CAR_TMA_W(WV)                                                   \
-  switch (vpt) {                                                        \
-    case 1: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 1>;       \
-    case 2: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 2>;       \
-    case 4: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 4>;       \
-    case 8: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 8>;       \
-    default: return nullptr;                                            \
+TmaFn pick_dt(int W, int vpt, int ls) {
+#define CAR_TMA_W(WV)                                                                          \
+  if (ls == kRegSlices) return vpt == 1   ? reduce_residual_rmsnorm_tma_kernel<DT, WV, 1, kRegSlices> \
+                               : vpt == 2 ? reduce_residual_rmsnorm_tma_kernel<DT, WV, 2, kRegSlices> \
+                                          : nullptr;                                           \
+  if (ls != 0) return nullptr;                                                                 \
+  switch (vpt) {                                                                               \
+    case 1: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 1, 0>;                           \
+    case 2: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 2, 0>;                           \
+    case 4: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 4, 0>;                           \
+    case 8: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 8, 0>;                           \
+    default: return nullptr;                                                                   \
   }
   switch (W) {
     case 2: CAR_TMA_W(2)
@@ -403,11 +456,11 @@ TmaFn pick_dt(int W, int vpt) {
 #undef CAR_TMA_W
 }
 
-TmaFn pick_tma(int dtype, int W, int vpt) {
+TmaFn pick_tma(int dtype, int W, int vpt, int ls) {
   switch (dtype) {
-    case kBF16: return pick_dt<kBF16>(W, vpt);
-    case kFP16: return pick_dt<kFP16>(W, vpt);
-    default: return pick_dt<kFP32>(W, vpt);
+    case kBF16: return pick_dt<kBF16>(W, vpt, ls);
+    case kFP16: return pick_dt<kFP16>(W, vpt, ls);
+    default: return pick_dt<kFP32>(W, vpt, ls);
   }
 }
 
@@ -417,7 +470,7 @@ TmaFn pick_tma(int dtype, int W, int vpt) {
 constexpr int kTmaSmemBudget = 200 * 1024;
 
 cudaError_t fused_tma_prepare(int dtype, int W, const FusedTmaShape& sh) {
-  TmaFn fn = pick_tma(dtype, W, sh.vpt);
+  TmaFn fn = pick_tma(dtype, W, sh.vpt, sh.ls);
   if (!fn) return cudaErrorInvalidValue;
   return cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               sh.smem);
@@ -435,14 +488,19 @@ bool fused_tma_shape(int64_t rows, int vec_per_row, int num_sms, int cluster, in
   if (vpt == 3) vpt = 4;
   if (vpt > 4 && vpt <= 8) vpt = 8;
   if (vpt > 8) return false;
-  // Ring depth: about one row's slices (W + 1, at least 6).  Deeper rings keep
-  // more bulk copies outstanding and measured slower on GB300 (W=8, N=8192
-  // bf16, M=512: 17.5 us with 9 slots, 17.9 us with 12 or 18).
-  int slots = W + 1 < 6 ? 6 : W + 1;
+  // The last kRegSlices slices of a row are loaded by the consumers when a
+  // thread holds at most two vectors (register room) and at least two slices
+  // are left for the ring.
+  const int ls = (vpt <= 2 && W + 1 - kRegSlices >= 2) ? kRegSlices : 0;
+  // Ring depth: about one row's bulk-copied slices (at least 6).  Deeper
+  // rings keep more bulk copies outstanding and measured slower on GB300
+  // (W=8, N=8192 bf16, M=512: 17.5 us with 9 slots, 17.9 us with 12 or 18).
+  int slots = W + 1 - ls < 6 ? 6 : W + 1 - ls;
   if (slots > kTmaSmemBudget / slice) slots = kTmaSmemBudget / slice;
   if (slots < 2) return false;
   const int64_t groups = num_sms / cluster;
   out->cluster = cluster;
+  out->ls = ls;
   out->consumers = consumers;
   out->vpt = vpt;
   out->slots = slots;
@@ -455,7 +513,7 @@ cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* r
                              float eps, void* residual_out, void* norm_out, void* ar_out, unsigned int* err,
                              int64_t rows, int64_t cols, int vec_per_row, const FusedTmaShape& sh,
                              cudaStream_t s) {
-  TmaFn fn = pick_tma(dtype, W, sh.vpt);
+  TmaFn fn = pick_tma(dtype, W, sh.vpt, sh.ls);
   if (!fn) return cudaErrorInvalidValue;
   TmaParams p;
   p.in = in;
@@ -471,6 +529,7 @@ cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* r
   p.row_bytes = vec_per_row * 16;
   p.vec_per_row = vec_per_row;
   p.slots = sh.slots;
+  p.tma_slices = W + 1 - sh.ls;
   p.consumers = sh.consumers;
   p.nranks = W;
   p.cluster = sh.cluster;
