@@ -488,10 +488,12 @@ bool fused_tma_shape(int64_t rows, int vec_per_row, int num_sms, int cluster, in
   if (vpt == 3) vpt = 4;
   if (vpt > 4 && vpt <= 8) vpt = 8;
   if (vpt > 8) return false;
-  // The last kRegSlices slices of a row are loaded by the consumers when a
-  // thread holds at most two vectors (register room) and at least two slices
-  // are left for the ring.
-  const int ls = (vpt <= 2 && W + 1 - kRegSlices >= 2) ? kRegSlices : 0;
+  // The last kRegSlices slices of a row are loaded by the consumers at W = 8
+  // when a thread holds at most two vectors (register room).  Measured on
+  // GB300 (N = 8192 bf16 unless noted), it pays only there: W = 8 M = 512
+  // 17.4 -> 17.0 us and M = 2048 57.5 -> 55.6 us, but W = 4 (M = 512 and
+  // 2048, also N = 4096 fp32), W = 6 and W = 16 were 2-10 % slower.
+  const int ls = (vpt <= 2 && W == 8) ? kRegSlices : 0;
   // Ring depth: about one row's bulk-copied slices (at least 6).  Deeper
   // rings keep more bulk copies outstanding and measured slower on GB300
   // (W=8, N=8192 bf16, M=512: 17.5 us with 9 slots, 17.9 us with 12 or 18).
