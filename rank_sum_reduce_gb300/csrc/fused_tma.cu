@@ -434,11 +434,15 @@ using TmaFn = void (*)(const TmaParams);
 
 template <int DT>
 TmaFn pick_dt(int W, int vpt, int ls) {
+  // register-loaded slices are used at W = 8 only (see fused_tma_shape)
+  if (ls == kRegSlices) {
+    if (W != 8) return nullptr;
+    return vpt == 1   ? reduce_residual_rmsnorm_tma_kernel<DT, 8, 1, kRegSlices>
+           : vpt == 2 ? reduce_residual_rmsnorm_tma_kernel<DT, 8, 2, kRegSlices>
+                      : nullptr;
+  }
+  if (ls != 0) return nullptr;
 #define CAR_TMA_W(WV)                                                                          \
-  if (ls == kRegSlices) return vpt == 1   ? reduce_residual_rmsnorm_tma_kernel<DT, WV, 1, kRegSlices> \
-                               : vpt == 2 ? reduce_residual_rmsnorm_tma_kernel<DT, WV, 2, kRegSlices> \
-                                          : nullptr;                                           \
-  if (ls != 0) return nullptr;                                                                 \
   switch (vpt) {                                                                               \
     case 1: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 1, 0>;                           \
     case 2: return reduce_residual_rmsnorm_tma_kernel<DT, WV, 2, 0>;                           \
