@@ -723,6 +723,45 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+PROFILE_CASES = {
+    # name: (W, M, N, dtype); each case's working set exceeds L2 and stays a few hundred MB
+    "ll128_decode": (16, 1024, 8192, "bf16"),
+    "ll_decode": (8, 512, 8192, "bf16"),
+    "fused_fp32": (4, 2048, 4096, "fp32"),
+}
+
+
+def profile_case(name, launches=4):
+    """Run one workload's kernel `launches` times and exit: a small, fixed
+    command for ncu captures of kernels outside the headline step."""
+    import torch
+
+    import rank_sum_reduce_gb300 as car
+
+    W, M, N, dt = PROFILE_CASES[name]
+    wl = workloads.custom(W, M, N, dt, seed=90)
+    dev = torch.device("cuda", 0)
+    xs = [workloads.make_x(wl, r, dev) for r in range(W)]
+    out = torch.empty_like(xs[0])
+    with car.Car(W, M, N, dt) as c:
+        if name == "fused_fp32":
+            res, w = workloads.make_residual(wl, dev), workloads.make_weight(wl, dev)
+            ro = torch.empty_like(res)
+            for _ in range(launches):
+                c.reduce_residual_rmsnorm(xs, res, w, wl.eps, ro, out)
+        else:
+            ll128 = name == "ll128_decode"
+            wb = c.ll128_wire_bytes if ll128 else c.ll_wire_bytes
+            wires = [torch.empty(wb, dtype=torch.uint8, device=dev) for _ in range(W)]
+            for x, wv in zip(xs, wires):
+                (c.ll128_encode if ll128 else c.ll_encode)(x, 7, wv)
+            for _ in range(launches):
+                (c.ll128_decode_reduce if ll128 else c.ll_decode_reduce)(wires, 7, out)
+        torch.cuda.synchronize()
+        c.sync()
+    print(f"profile case {name}: W={W} M={M} N={N} {dt}, {launches} launches")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -731,7 +770,12 @@ def main():
     ap.add_argument("--impl", choices=["car", "reference"], default="car")
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="run one workload's kernel a few times and exit (for ncu captures)")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
