@@ -48,6 +48,13 @@ MUTANTS = [
     ("two_shot_no_rotation", "      const int r = (int)((owner + k) % W);", "      const int r = k;"),
     ("two_shot_no_remainder_owner", "    if (owner > W - 1) owner = W - 1;  /* the last rank takes the remainder */",
      "    if (owner > W - 1) owner = 0;"),
+    ("lamport_no_scrub", "    if (v == 0x8000u) v = 0;  /* scrub -0.0 */", "    (void)0;"),
+    ("lamport_reads_next_region", "  const uint8_t* region = base + (int64_t)(round % 3) * region_bytes;",
+     "  const uint8_t* region = base + (int64_t)((round + 1) % 3) * region_bytes;"),
+    ("lamport_refills_next_region", "  orc_lamport_fill(base + (int64_t)((round + 2) % 3) * region_bytes, region_bytes / 4);",
+     "  orc_lamport_fill(base + (int64_t)((round + 1) % 3) * region_bytes, region_bytes / 4);"),
+    ("lamport_stale_row_not_zeroed", "      memset((uint8_t*)residual_out + 2 * m * N, 0, (size_t)(2 * N));", ""),
+    ("lamport_checks_first_word_only", "      for (int64_t j = 0; j < N; j += 2) {", "      for (int64_t j = 0; j < 2; j += 2) {"),
 ]
 
 
@@ -71,6 +78,9 @@ def battery(orc):
         ("single_stale_ll", lambda: pins.test_each_single_stale_line_detected_alone(orc, "ll")),
         ("ll_flag2", lambda: pins.test_ll_second_flag_alone_is_checked(orc)),
         ("two_shot_rotation", lambda: pins.test_two_shot_is_rotated_one_shot_per_shard(orc, 5, 23)),
+        ("lamport_push_brute_force", lambda: pins.test_lamport_push_never_writes_the_sentinel(orc)),
+        ("lamport_round", lambda: pins.test_lamport_round_equals_fused_op_on_scrubbed_inputs(orc)),
+        ("lamport_missing_word", lambda: pins.test_lamport_missing_word_makes_its_row_stale(orc, (1, 2, 128))),
     ]
 
 
