@@ -554,6 +554,23 @@ def ll128_row(arm, iters=10):
             "stale_reported": n_stale, "stale_planted": len(planted), "stale_set_matches": bool(ok)}
 
 
+# the (M, N) shapes of the fused op's latency table in "用 Triton + Symmetric
+# Memory 写一个 AllReduce + RMSNorm 融合算子" (measured there on four GPUs
+# over NVLink, so context only)
+PAGE_SHAPES = [(1, 2048), (8, 2048), (128, 2048), (1, 4096), (128, 4096), (1, 8192), (128, 8192)]
+
+
+def page_shapes_row(arm):
+    """µs per call of the fused op (W=4 bf16, residual_out + norm_out) at the
+    page table's shapes, from CUDA-graph replay over cold buffer sets."""
+    out = {}
+    for M, N in PAGE_SHAPES:
+        wl = workloads.custom(4, M, N, "bf16", seed=100 + M + N)
+        r = latency_row(arm, wl, 2, calls=4000)
+        out[f"m{M}_n{N}"] = {"us_per_call": r["us_per_call"], "GBps": r["GBps"]}
+    return {"W": 4, "dtype": "bf16", "outputs": 2, "shapes": out}
+
+
 def ll128_misaligned_row(arm, M, launches, reps=5):
     """LL128 encode and decode-reduce at W=8, N=8192 bf16 (M rows per rank)
     with the rank data and the output 16-byte aligned, then both at 4, 8 and
@@ -811,6 +828,7 @@ def main():
         rows["two_shot_m512_w8"] = two_shot_row(arm)
         rows["ll128_w16_decode_reduce"] = ll128_row(arm)
         rows["ll_m512_w8"] = ll_row(arm)
+        rows["fused_w4_page_shapes"] = page_shapes_row(arm)
         rows["ll128_misaligned_1MiB"] = ll128_misaligned_row(arm, 64, 256)
         rows["ll128_misaligned_64MiB"] = ll128_misaligned_row(arm, 4096, 16)
         torch.cuda.empty_cache()

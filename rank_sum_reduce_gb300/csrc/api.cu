@@ -144,7 +144,13 @@ car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
     }
   }
   int c = 1;
-  if (M < 2 * (int64_t)num_sms) {
+  if (M == 1) {
+    // One row: measured on GB300 (bf16, W = 2..16), a cluster of two never
+    // paid for its barrier; up to 512 vectors one CTA was fastest (W = 4,
+    // N = 4096: 2.32 against 2.68 us with two), from 1024 vectors a cluster
+    // of eight (W = 2, N = 8192: 2.64 against 2.90 us with two).
+    c = V > 512 ? 8 : 1;
+  } else if (M < 2 * (int64_t)num_sms) {
     const int64_t row_input_bytes = (int64_t)(W + 1) * V * 16;
     while (c < 8 && row_input_bytes / c > 24 * 1024 && (int64_t)c * M < num_sms) c *= 2;
   }
