@@ -135,30 +135,23 @@ int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
 //    (measured on GB300: W=2, N=2048 bf16 runs best on one CTA, W=8,
 //    N=8192 bf16 on eight).
 car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
-  car::FusedShape sh{1, 32, 1, 1};
-  if (M >= 2 * (int64_t)num_sms) {
+  // Measured on GB300 (bf16, W = 2..16, M = 1..128, N = 2048..8192): a
+  // cluster of two never paid for its barrier.  A few wide rows (more than
+  // 512 vectors, 8 M <= SMs) ran fastest split over eight CTAs (W = 2, M = 1,
+  // N = 8192: 2.64 against 2.90 us with two; W = 8, M = 8, N = 8192: 3.04
+  // against 3.48 us with one), every other shape with one CTA per row and one
+  // or two vectors per thread (W = 8, M = 128, N = 8192: 6.00 against 8.25 us
+  // with two CTAs per row).  A row too wide for one CTA's threads takes the
+  // smallest cluster whose CTAs cover it.
+  for (int c = (V > 512 && 8 * M <= num_sms) ? 8 : 1; c <= 8; c *= 2) {
+    const int chunk = (V + c - 1) / c;
     for (int vpt = 1; vpt <= 2; vpt++) {
       if (!car::fused_has_variant(W, vpt)) continue;
-      const int t = round_up32((V + vpt - 1) / vpt);
-      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{1, t, vpt, 1};
+      const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
+      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{c, t, vpt, 1};
     }
   }
-  int c = 1;
-  if (M == 1) {
-    // One row: measured on GB300 (bf16, W = 2..16), a cluster of two never
-    // paid for its barrier; up to 512 vectors one CTA was fastest (W = 4,
-    // N = 4096: 2.32 against 2.68 us with two), from 1024 vectors a cluster
-    // of eight (W = 2, N = 8192: 2.64 against 2.90 us with two).
-    c = V > 512 ? 8 : 1;
-  } else if (M < 2 * (int64_t)num_sms) {
-    const int64_t row_input_bytes = (int64_t)(W + 1) * V * 16;
-    while (c < 8 && row_input_bytes / c > 24 * 1024 && (int64_t)c * M < num_sms) c *= 2;
-  }
-  while (c < 8 && (V + c - 1) / c > car::fused_max_threads(W, 1)) c *= 2;
-  sh.cluster = c;
-  sh.vpt = 1;
-  sh.threads = std::max(32, round_up32((V + c - 1) / c));
-  return sh;
+  return car::FusedShape{8, std::max(32, round_up32((V + 7) / 8)), 1, 1};  // rows past CAR_MAX_ROW_BYTES only
 }
 
 bool shape_valid(int W, int V, const car::FusedShape& sh) {
@@ -169,11 +162,13 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
   return (int64_t)sh.threads * sh.vpt >= chunk;
 }
 
-// The pipelined kernel is faster once every SM has a row to stream (measured
-// on GB300 at W=8, N=8192 bf16 and W=4, N=4096 fp32, M >= 304); below that
-// the row-split kernel spreads the few rows over more SMs.
+// The pipelined kernel is faster once every SM has one and a half rows to
+// stream.  Measured on GB300 against the row kernel with one CTA per row:
+// W = 8 N = 8192 bf16 at M = 152, 6.5 (rows) against 7.4 us (pipeline); at
+// M = 200 mixed (W = 8: 9.5 against 9.8, W = 4: 7.3 against 7.1); from M = 228
+// the pipeline wins (W = 8: 10.0 against 10.3, M = 456: 14.6 against 16.9).
 int auto_fused_kernel(const car_ctx* h) {
-  return (h->tma_ok && h->M >= (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
+  return (h->tma_ok && 2 * h->M >= 3 * (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
 }
 
 // Row-kernel shape for the Lamport receive step: the same rules as the fused
