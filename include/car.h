@@ -23,7 +23,9 @@
  *   boundary (P1 "线程模型：16 字节一个单位": the message is processed in
  *   16-byte packed units; P3 "2. 线程怎么分活").
  * - Pointers.  "dev" pointers are device memory on the handle's device,
- *   owned by the caller, and must be 16-byte aligned.  Pointer tables
+ *   owned by the caller, and must be 16-byte aligned unless the call states
+ *   otherwise (the LL128 data and outputs need only element alignment).
+ *   Pointer tables
  *   (inputs, wires) are host arrays of W device pointers, read during the
  *   call only.  The library never frees caller memory.
  * - Streams.  `stream` is a cudaStream_t passed as void*; NULL is the legacy
