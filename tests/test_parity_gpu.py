@@ -155,6 +155,10 @@ FUSED_CASES = [
     (3, 5, 1544, "fp16"), (16, 2, 4096, "bf16"), (4, 7, 4096, "fp32"), (1, 9, 264, "bf16"),
     (5, 331, 776, "fp32"), (8, 310, 8192, "bf16"), (2, 1, 8, "bf16"), (7, 2, 16, "fp16"),
     (8, 2, 32768, "bf16"), (4, 1, 16384, "fp32"),
+    # row kernel between a few rows and the pipeline's threshold: one CTA per
+    # row with two vectors per thread (W=8), 1024 threads (W=4), a cluster of
+    # two where no two-vector instance exists (W=16)
+    (8, 64, 8192, "bf16"), (8, 180, 8192, "bf16"), (4, 150, 8192, "bf16"), (16, 40, 8192, "bf16"),
 ]
 
 
