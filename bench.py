@@ -490,17 +490,19 @@ def two_shot_row(arm, iters=200):
 
 
 def lamport_row(arm, wl, rounds=30, reps=20):
-    """Lamport one-shot push at M=1: µs per receive (fused residual + RMSNorm,
-    sentinel checks and refill of the previous region) and µs per round (W
-    pushes + the receive), from graph replay; small enough to stay in L2."""
+    """Lamport one-shot push at M=1, from graph replay, small enough to stay in
+    L2: µs per round (W pushes + the receive: fused residual + RMSNorm,
+    sentinel checks, refill of the previous region) on one receive buffer, and
+    µs per receive alone.  For the latter, round j reads its own buffer, filled
+    beforehand by that round's pushes: a receive refills another region of
+    it, so every replay reads complete data (a receive-only sequence on one
+    buffer would read regions its predecessors had just refilled)."""
     torch, car = arm.torch, arm.car
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
-    comm = torch.empty(c.lamport_buffer_bytes, dtype=torch.uint8, device=arm.dev)
     xs, res, w = workloads.make_inputs(wl, arm.dev)
     ro, no = torch.empty_like(res), torch.empty_like(res)
-    c.lamport_init(comm)
 
-    def round_fn(j, push):
+    def round_fn(j, push, comm):
         def run(stream):
             if push:
                 for r, x in enumerate(xs):
@@ -508,17 +510,28 @@ def lamport_row(arm, wl, rounds=30, reps=20):
             c.lamport_reduce_residual_rmsnorm(comm, j, res, w, wl.eps, ro, no, stream=stream)
         return run
 
-    full = capture(torch, [round_fn(j, True) for j in range(rounds)])
-    recv = capture(torch, [round_fn(j, False) for j in range(rounds)])
+    comm = torch.empty(c.lamport_buffer_bytes, dtype=torch.uint8, device=arm.dev)
+    c.lamport_init(comm)
+    full = capture(torch, [round_fn(j, True, comm) for j in range(rounds)])
     full.replay()
     n_stale, _ = c.lamport_report()
     per_round = timed(torch, lambda i: full.replay(), reps) * 1000.0 / rounds
+    del full
+    bufs = [torch.empty(c.lamport_buffer_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(rounds)]
+    for j, b in enumerate(bufs):
+        c.lamport_init(b)
+        for r, x in enumerate(xs):
+            c.lamport_push(x, r, j, b)
+    recv = capture(torch, [round_fn(j, False, bufs[j]) for j in range(rounds)])
+    recv.replay()
+    n_stale_recv, _ = c.lamport_report()
     per_recv = timed(torch, lambda i: recv.replay(), reps) * 1000.0 / rounds
-    del full, recv
+    del recv, bufs
     c.close()
     return {"workload": "lamport_" + wl.name, "us_per_receive": round(per_recv, 3),
             "us_per_round_with_pushes": round(per_round, 3), "kernels_per_round": wl.W + 1,
-            "stale_after_full_round": n_stale, "l2": "warm (buffers fit in L2)"}
+            "stale_after_full_round": n_stale, "stale_after_receives": n_stale_recv,
+            "l2": "warm (buffers fit in L2)"}
 
 
 def fused_fp32_row(arm, iters=50):
