@@ -24,6 +24,7 @@ CAR_FUSED_AUTO, CAR_FUSED_ROWS, CAR_FUSED_PIPELINE = 0, 1, 2
 CAR_STALE_LIST_MAX = 65536
 CAR_MAX_ROW_BYTES = 64 * 1024
 DTYPE_CODE = {"bf16": CAR_BF16, "fp16": CAR_FP16, "fp32": CAR_FP32}
+ELEM_SIZE = {"bf16": 2, "fp16": 2, "fp32": 4}
 STATUS_NAME = {CAR_OK: "CAR_OK", CAR_ERR_ARG: "CAR_ERR_ARG", CAR_ERR_ALIGN: "CAR_ERR_ALIGN",
                CAR_ERR_SIZE: "CAR_ERR_SIZE", CAR_ERR_CUDA: "CAR_ERR_CUDA",
                CAR_ERR_STALE_FLAG: "CAR_ERR_STALE_FLAG", CAR_ERR_HANDLE: "CAR_ERR_HANDLE",
@@ -230,13 +231,36 @@ def _stream(stream):
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
+def _ptr(t, nbytes: int, what: str) -> int:
+    """Device pointer of a tensor the library will read or write `nbytes` of:
+    it must be a contiguous CUDA tensor at least that large (any dtype: the
+    library sees bytes)."""
+    if not t.is_cuda:
+        raise ValueError(f"{what}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{what}: {t.numel() * t.element_size()} bytes, the call needs {nbytes}")
+    return t.data_ptr()
+
+
 class Car:
-    """A libcar handle for W rank buffers of [M, N] elements of one dtype."""
+    """A libcar handle for W rank buffers of [M, N] elements of one dtype.
+
+    The methods take torch tensors and pass their device pointers to the C
+    ABI; each tensor must be a contiguous CUDA tensor of at least the bytes
+    the call reads or writes (ValueError otherwise)."""
 
     def __init__(self, W: int, M: int, N: int, dtype: str):
         st, h = car_create(W, M, N, DTYPE_CODE[dtype])
         check(st, "car_create")
         self.h, self.W, self.M, self.N, self.dtype = h, W, M, N, dtype
+        self.D = M * N * ELEM_SIZE[dtype]      # bytes per rank
+
+    def _ranks(self, ts, nbytes: int, what: str):
+        if len(ts) != self.W:
+            raise ValueError(f"{what}: {len(ts)} tensors for W = {self.W}")
+        return [_ptr(t, nbytes, f"{what}[{r}]") for r, t in enumerate(ts)]
 
     def close(self):
         if self.h is not None:
@@ -264,24 +288,29 @@ class Car:
         return car_ll_wire_bytes(self.h)
 
     def reduce(self, xs, ar_out, stream=None):
-        check(car_reduce(self.h, [x.data_ptr() for x in xs], ar_out.data_ptr(), _stream(stream)), "car_reduce")
+        check(car_reduce(self.h, self._ranks(xs, self.D, "inputs"), _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+              "car_reduce")
 
     def reduce_two_shot(self, xs, ar_out, stream=None):
-        check(car_reduce_two_shot(self.h, [x.data_ptr() for x in xs], ar_out.data_ptr(), _stream(stream)),
-              "car_reduce_two_shot")
+        check(car_reduce_two_shot(self.h, self._ranks(xs, self.D, "inputs"), _ptr(ar_out, self.D, "ar_out"),
+                                  _stream(stream)), "car_reduce_two_shot")
 
     def reduce_residual_rmsnorm(self, xs, residual, weight, eps, residual_out, norm_out, ar_out=None, stream=None):
-        check(car_reduce_residual_rmsnorm(self.h, [x.data_ptr() for x in xs], residual.data_ptr(),
-                                          weight.data_ptr(), eps, residual_out.data_ptr(), norm_out.data_ptr(),
-                                          ar_out.data_ptr() if ar_out is not None else None, _stream(stream)),
-              "car_reduce_residual_rmsnorm")
+        D = self.D
+        check(car_reduce_residual_rmsnorm(self.h, self._ranks(xs, D, "inputs"), _ptr(residual, D, "residual"),
+                                          _ptr(weight, D // self.M, "weight"), eps,
+                                          _ptr(residual_out, D, "residual_out"), _ptr(norm_out, D, "norm_out"),
+                                          _ptr(ar_out, D, "ar_out") if ar_out is not None else None,
+                                          _stream(stream)), "car_reduce_residual_rmsnorm")
 
     def ll128_encode(self, data, flag, wire, stream=None):
-        check(car_ll128_encode(self.h, data.data_ptr(), flag, wire.data_ptr(), _stream(stream)), "car_ll128_encode")
+        check(car_ll128_encode(self.h, _ptr(data, self.D, "data"), flag, _ptr(wire, self.ll128_wire_bytes, "wire"),
+                               _stream(stream)), "car_ll128_encode")
 
     def ll128_decode_reduce(self, wires, expected_flag, ar_out, max_polls=1, stream=None):
-        check(car_ll128_decode_reduce(self.h, [w.data_ptr() for w in wires], expected_flag, max_polls,
-                                      ar_out.data_ptr(), _stream(stream)), "car_ll128_decode_reduce")
+        check(car_ll128_decode_reduce(self.h, self._ranks(wires, self.ll128_wire_bytes, "wires"), expected_flag,
+                                      max_polls, _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+              "car_ll128_decode_reduce")
 
     def ll128_report(self, cap=CAR_STALE_LIST_MAX):
         st, n, pairs = car_ll128_report(self.h, cap)
@@ -290,11 +319,13 @@ class Car:
         return n, pairs
 
     def ll_encode(self, data, flag, wire, stream=None):
-        check(car_ll_encode(self.h, data.data_ptr(), flag, wire.data_ptr(), _stream(stream)), "car_ll_encode")
+        check(car_ll_encode(self.h, _ptr(data, self.D, "data"), flag, _ptr(wire, self.ll_wire_bytes, "wire"),
+                            _stream(stream)), "car_ll_encode")
 
     def ll_decode_reduce(self, wires, expected_flag, ar_out, max_polls=1, stream=None):
-        check(car_ll_decode_reduce(self.h, [w.data_ptr() for w in wires], expected_flag, max_polls,
-                                   ar_out.data_ptr(), _stream(stream)), "car_ll_decode_reduce")
+        check(car_ll_decode_reduce(self.h, self._ranks(wires, self.ll_wire_bytes, "wires"), expected_flag,
+                                   max_polls, _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+              "car_ll_decode_reduce")
 
     def ll_report(self, cap=CAR_STALE_LIST_MAX):
         st, n, pairs = car_ll_report(self.h, cap)
@@ -307,18 +338,22 @@ class Car:
         return car_lamport_buffer_bytes(self.h)
 
     def lamport_init(self, comm, stream=None):
-        check(car_lamport_init(self.h, comm.data_ptr(), _stream(stream)), "car_lamport_init")
+        check(car_lamport_init(self.h, _ptr(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)),
+              "car_lamport_init")
 
     def lamport_push(self, data, rank, round_, comm, stream=None):
-        check(car_lamport_push(self.h, data.data_ptr(), rank, round_, comm.data_ptr(), _stream(stream)),
-              "car_lamport_push")
+        check(car_lamport_push(self.h, _ptr(data, self.D, "data"), rank, round_,
+                               _ptr(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)), "car_lamport_push")
 
     def lamport_reduce_residual_rmsnorm(self, comm, round_, residual, weight, eps, residual_out, norm_out,
                                         ar_out=None, max_polls=1, stream=None):
-        check(car_lamport_reduce_residual_rmsnorm(self.h, comm.data_ptr(), round_, max_polls, residual.data_ptr(),
-                                                  weight.data_ptr(), eps, residual_out.data_ptr(),
-                                                  norm_out.data_ptr(), ar_out.data_ptr() if ar_out is not None
-                                                  else None, _stream(stream)), "car_lamport_reduce_residual_rmsnorm")
+        D = self.D
+        check(car_lamport_reduce_residual_rmsnorm(self.h, _ptr(comm, self.lamport_buffer_bytes, "comm"), round_,
+                                                  max_polls, _ptr(residual, D, "residual"),
+                                                  _ptr(weight, D // self.M, "weight"), eps,
+                                                  _ptr(residual_out, D, "residual_out"), _ptr(norm_out, D, "norm_out"),
+                                                  _ptr(ar_out, D, "ar_out") if ar_out is not None else None,
+                                                  _stream(stream)), "car_lamport_reduce_residual_rmsnorm")
 
     def lamport_report(self, cap=CAR_STALE_LIST_MAX):
         st, n, pairs = car_lamport_report(self.h, cap)

@@ -279,6 +279,29 @@ def test_fused_rejects_rows_beyond_limit(car):
         assert st == car.CAR_ERR_SIZE
 
 
+def test_binding_rejects_unusable_tensors(car):
+    """The torch layer checks what it hands the C ABI: CUDA, contiguous, and at
+    least the bytes the call touches; the rank list has W entries."""
+    W, M, N = 2, 4, 256
+    xs = [torch.zeros(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(W)]
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    with car.Car(W, M, N, "bf16") as c:
+        with pytest.raises(ValueError, match="CUDA"):
+            c.reduce([xs[0].cpu(), xs[1]], out)
+        with pytest.raises(ValueError, match="contiguous"):
+            c.reduce([xs[0], torch.zeros(N, M, dtype=torch.bfloat16, device=DEV).t()], out)
+        with pytest.raises(ValueError, match="needs"):
+            c.reduce(xs, out.view(-1)[:-1])
+        with pytest.raises(ValueError, match="W = 2"):
+            c.reduce(xs[:1], out)
+        wire = torch.empty(c.ll128_wire_bytes - 16, dtype=torch.uint8, device=DEV)
+        with pytest.raises(ValueError, match="wire"):
+            c.ll128_encode(xs[0], 7, wire)
+        c.reduce(xs, out)   # a valid call still works
+    torch.cuda.synchronize()
+    assert bool((out == 0).all())
+
+
 def test_argument_errors_launch_nothing(car):
     with car.Car(2, 2, 64, "bf16") as c:
         x = torch.zeros(2 * 64 + 8, dtype=torch.bfloat16, device=DEV)
