@@ -231,12 +231,14 @@ def _stream(stream):
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
-def _ptr(t, nbytes: int, what: str) -> int:
+def _ptr(t, nbytes: int, what: str, device=None) -> int:
     """Device pointer of a tensor the library will read or write `nbytes` of:
-    it must be a contiguous CUDA tensor at least that large (any dtype: the
-    library sees bytes)."""
+    it must be a contiguous CUDA tensor at least that large, on `device` when
+    given (any dtype: the library sees bytes)."""
     if not t.is_cuda:
         raise ValueError(f"{what}: expected a CUDA tensor")
+    if device is not None and t.device.index != device:
+        raise ValueError(f"{what}: on cuda:{t.device.index}, the handle is on cuda:{device}")
     if not t.is_contiguous():
         raise ValueError(f"{what}: expected a contiguous tensor")
     if t.numel() * t.element_size() < nbytes:
@@ -256,11 +258,17 @@ class Car:
         check(st, "car_create")
         self.h, self.W, self.M, self.N, self.dtype = h, W, M, N, dtype
         self.D = M * N * ELEM_SIZE[dtype]      # bytes per rank
+        import torch
+
+        self.device = torch.cuda.current_device()
+
+    def _p(self, t, nbytes: int, what: str) -> int:
+        return _ptr(t, nbytes, what, self.device)
 
     def _ranks(self, ts, nbytes: int, what: str):
         if len(ts) != self.W:
             raise ValueError(f"{what}: {len(ts)} tensors for W = {self.W}")
-        return [_ptr(t, nbytes, f"{what}[{r}]") for r, t in enumerate(ts)]
+        return [self._p(t, nbytes, f"{what}[{r}]") for r, t in enumerate(ts)]
 
     def close(self):
         if self.h is not None:
@@ -288,28 +296,28 @@ class Car:
         return car_ll_wire_bytes(self.h)
 
     def reduce(self, xs, ar_out, stream=None):
-        check(car_reduce(self.h, self._ranks(xs, self.D, "inputs"), _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+        check(car_reduce(self.h, self._ranks(xs, self.D, "inputs"), self._p(ar_out, self.D, "ar_out"), _stream(stream)),
               "car_reduce")
 
     def reduce_two_shot(self, xs, ar_out, stream=None):
-        check(car_reduce_two_shot(self.h, self._ranks(xs, self.D, "inputs"), _ptr(ar_out, self.D, "ar_out"),
+        check(car_reduce_two_shot(self.h, self._ranks(xs, self.D, "inputs"), self._p(ar_out, self.D, "ar_out"),
                                   _stream(stream)), "car_reduce_two_shot")
 
     def reduce_residual_rmsnorm(self, xs, residual, weight, eps, residual_out, norm_out, ar_out=None, stream=None):
         D = self.D
-        check(car_reduce_residual_rmsnorm(self.h, self._ranks(xs, D, "inputs"), _ptr(residual, D, "residual"),
-                                          _ptr(weight, D // self.M, "weight"), eps,
-                                          _ptr(residual_out, D, "residual_out"), _ptr(norm_out, D, "norm_out"),
-                                          _ptr(ar_out, D, "ar_out") if ar_out is not None else None,
+        check(car_reduce_residual_rmsnorm(self.h, self._ranks(xs, D, "inputs"), self._p(residual, D, "residual"),
+                                          self._p(weight, D // self.M, "weight"), eps,
+                                          self._p(residual_out, D, "residual_out"), self._p(norm_out, D, "norm_out"),
+                                          self._p(ar_out, D, "ar_out") if ar_out is not None else None,
                                           _stream(stream)), "car_reduce_residual_rmsnorm")
 
     def ll128_encode(self, data, flag, wire, stream=None):
-        check(car_ll128_encode(self.h, _ptr(data, self.D, "data"), flag, _ptr(wire, self.ll128_wire_bytes, "wire"),
+        check(car_ll128_encode(self.h, self._p(data, self.D, "data"), flag, self._p(wire, self.ll128_wire_bytes, "wire"),
                                _stream(stream)), "car_ll128_encode")
 
     def ll128_decode_reduce(self, wires, expected_flag, ar_out, max_polls=1, stream=None):
         check(car_ll128_decode_reduce(self.h, self._ranks(wires, self.ll128_wire_bytes, "wires"), expected_flag,
-                                      max_polls, _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+                                      max_polls, self._p(ar_out, self.D, "ar_out"), _stream(stream)),
               "car_ll128_decode_reduce")
 
     def ll128_report(self, cap=CAR_STALE_LIST_MAX):
@@ -319,12 +327,12 @@ class Car:
         return n, pairs
 
     def ll_encode(self, data, flag, wire, stream=None):
-        check(car_ll_encode(self.h, _ptr(data, self.D, "data"), flag, _ptr(wire, self.ll_wire_bytes, "wire"),
+        check(car_ll_encode(self.h, self._p(data, self.D, "data"), flag, self._p(wire, self.ll_wire_bytes, "wire"),
                             _stream(stream)), "car_ll_encode")
 
     def ll_decode_reduce(self, wires, expected_flag, ar_out, max_polls=1, stream=None):
         check(car_ll_decode_reduce(self.h, self._ranks(wires, self.ll_wire_bytes, "wires"), expected_flag,
-                                   max_polls, _ptr(ar_out, self.D, "ar_out"), _stream(stream)),
+                                   max_polls, self._p(ar_out, self.D, "ar_out"), _stream(stream)),
               "car_ll_decode_reduce")
 
     def ll_report(self, cap=CAR_STALE_LIST_MAX):
@@ -338,21 +346,21 @@ class Car:
         return car_lamport_buffer_bytes(self.h)
 
     def lamport_init(self, comm, stream=None):
-        check(car_lamport_init(self.h, _ptr(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)),
+        check(car_lamport_init(self.h, self._p(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)),
               "car_lamport_init")
 
     def lamport_push(self, data, rank, round_, comm, stream=None):
-        check(car_lamport_push(self.h, _ptr(data, self.D, "data"), rank, round_,
-                               _ptr(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)), "car_lamport_push")
+        check(car_lamport_push(self.h, self._p(data, self.D, "data"), rank, round_,
+                               self._p(comm, self.lamport_buffer_bytes, "comm"), _stream(stream)), "car_lamport_push")
 
     def lamport_reduce_residual_rmsnorm(self, comm, round_, residual, weight, eps, residual_out, norm_out,
                                         ar_out=None, max_polls=1, stream=None):
         D = self.D
-        check(car_lamport_reduce_residual_rmsnorm(self.h, _ptr(comm, self.lamport_buffer_bytes, "comm"), round_,
-                                                  max_polls, _ptr(residual, D, "residual"),
-                                                  _ptr(weight, D // self.M, "weight"), eps,
-                                                  _ptr(residual_out, D, "residual_out"), _ptr(norm_out, D, "norm_out"),
-                                                  _ptr(ar_out, D, "ar_out") if ar_out is not None else None,
+        check(car_lamport_reduce_residual_rmsnorm(self.h, self._p(comm, self.lamport_buffer_bytes, "comm"), round_,
+                                                  max_polls, self._p(residual, D, "residual"),
+                                                  self._p(weight, D // self.M, "weight"), eps,
+                                                  self._p(residual_out, D, "residual_out"), self._p(norm_out, D, "norm_out"),
+                                                  self._p(ar_out, D, "ar_out") if ar_out is not None else None,
                                                   _stream(stream)), "car_lamport_reduce_residual_rmsnorm")
 
     def lamport_report(self, cap=CAR_STALE_LIST_MAX):
