@@ -248,6 +248,57 @@ def test_fused_pipeline_many_rows(car, W, M, N, dtype, cluster):
     assert_norm_close(no[rows], ref_no)
 
 
+def _degenerate_rows(W, M, N, seed):
+    """bf16 inputs whose rows 0..4 are degenerate cases of the fused op, the
+    rest ordinary: 0 all zero; 1 zero inputs over a constant residual; 2 every
+    rank -0.0; 3 +inf in one rank; 4 zero inputs and residual (for eps = 0)."""
+    g = torch.Generator().manual_seed(seed)
+    xs = [torch.randn(M, N, generator=g).bfloat16() for _ in range(W)]
+    res = torch.randn(M, N, generator=g).bfloat16()
+    w = (torch.rand(N, generator=g) + 0.5).bfloat16()
+    for x in xs:
+        x[0] = 0.0
+        x[1] = 0.0
+        x[2] = -0.0
+        x[4] = 0.0
+    res[0] = 0.0
+    res[1] = 0.375
+    res[4] = 0.0
+    xs[W - 1][3, N // 2] = float("inf")
+    return xs, res, w
+
+
+@pytest.mark.parametrize("kernel,M", [("rows", 6), ("pipeline", 300)])
+@pytest.mark.parametrize("eps", [1e-6, 0.0])
+def test_fused_degenerate_rows(car, kernel, M, eps):
+    """ar and residual_out bit-exact, norm_out within tolerance, and NaN in
+    exactly the same places as the oracle (inf inputs; a zero row with eps 0)."""
+    W, N = 3, 1024
+    xs, res, w = _degenerate_rows(W, M, N, seed=77 + M)
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, eps, M, N, "bf16")
+    dx = [x.to(DEV) for x in xs]
+    ro, no, ar = (torch.empty(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(3))
+    with car.Car(W, M, N, "bf16") as c:
+        c.tune_fused(car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE)
+        c.reduce_residual_rmsnorm(dx, res.to(DEV), w.to(DEV), eps, ro, no, ar)
+    torch.cuda.synchronize()
+    assert_bits_equal(ar, ref_ar, "ar")
+    assert_bits_equal(ro, ref_ro, "residual_out")
+    got, ref = no.cpu().float(), ref_no.float()
+    assert torch.equal(torch.isnan(got), torch.isnan(ref)), "NaN positions differ"
+    # inf in one element: the row's statistic is inf, so rms = 0; that element
+    # gives inf * 0 = NaN, every other element of the row 0
+    assert bool(torch.isnan(ref[3, N // 2])) and int(torch.isnan(ref[3]).sum()) == 1
+    assert bool((got[3][~torch.isnan(got[3])] == 0).all())
+    assert bits(ar)[2].eq(-32768).all()                         # -0.0 ranks sum to -0.0 (seeded with rank 0)
+    if eps > 0:
+        assert bool((ref[0] == 0).all()) and bool((got[0] == 0).all())   # zero row: exactly 0
+    else:
+        assert bool(torch.isnan(ref[0]).all()) and bool(torch.isnan(ref[4]).all())  # 0 * rsqrt(0)
+    keep = ~torch.isnan(ref)
+    assert_norm_close(got[keep], ref[keep])
+
+
 def test_fused_aliasing_and_no_ar(car):
     W, M, N = 4, 6, 2048
     wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=31)
