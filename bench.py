@@ -327,35 +327,46 @@ def headline(arm, wl, steps, warmup, rank, world):
 
 def e2e(arm, wl, steps, warmup, streams=1):
     """Same step through the public API with pinned host buffers: H2D of the
-    step's inputs, the two calls, D2H of its three outputs, all timed.  With
-    streams > 1, step i runs on stream i % streams with that stream's own
-    device and host buffers, so one step's copies overlap the neighbouring
-    steps' copies and kernels (the copy engines work in both directions at
-    once); every step still copies all of its inputs in and outputs out."""
+    step's inputs, the two calls, D2H of its three outputs, all timed.  The
+    inputs (W ranks, residual, weight) sit in one pinned host buffer and one
+    device buffer, and the outputs in one of each, so a step makes one copy
+    each way (the copy engines charge a gap per copy).  With streams > 1,
+    step i runs on stream i % streams with that stream's own device and host
+    buffers, so one step's copies overlap the neighbouring steps' copies and
+    kernels; every step still copies all of its inputs in and outputs out."""
     torch, car = arm.torch, arm.car
     dev = arm.dev
     xs, res, w = workloads.make_inputs(wl, dev)
-    hx = [x.cpu().pin_memory() for x in xs]
-    hres, hw = res.cpu().pin_memory(), w.cpu().pin_memory()
+    parts = xs + [res, w]
+    sizes = [t.numel() * t.element_size() for t in parts]   # each a multiple of 16 bytes
+    offs = [sum(sizes[:i]) for i in range(len(sizes))]
+    total = sum(sizes)
+    hin = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o, n in zip(parts, offs, sizes):
+        hin[o:o + n].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    D = wl.data_bytes
+
+    def views(buf, like):
+        return [buf[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(like, offs, sizes)]
+
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
     lanes = []
     for _ in range(streams):
+        din = torch.empty(total, dtype=torch.uint8, device=dev)
+        dout = torch.empty(3 * D, dtype=torch.uint8, device=dev)
+        v = views(din, parts)
+        outs = [dout[k * D:(k + 1) * D].view(res.dtype).view(res.shape) for k in range(3)]
         lanes.append({"stream": torch.cuda.Stream() if streams > 1 else torch.cuda.current_stream(),
-                      "dx": [torch.empty_like(x) for x in xs], "dres": torch.empty_like(res),
-                      "dw": torch.empty_like(w), "outs": [torch.empty_like(res) for _ in range(3)],
-                      "houts": [torch.empty_like(hres).pin_memory() for _ in range(3)]})
+                      "din": din, "dout": dout, "dx": v[:wl.W], "dres": v[wl.W], "dw": v[wl.W + 1], "outs": outs,
+                      "hout": torch.empty(3 * D, dtype=torch.uint8).pin_memory()})
 
     def step(i):
         L = lanes[i % streams]
         with torch.cuda.stream(L["stream"]):
-            for d, hsrc in zip(L["dx"], hx):
-                d.copy_(hsrc, non_blocking=True)
-            L["dres"].copy_(hres, non_blocking=True)
-            L["dw"].copy_(hw, non_blocking=True)
+            L["din"].copy_(hin, non_blocking=True)
             c.reduce(L["dx"], L["outs"][0])
             c.reduce_residual_rmsnorm(L["dx"], L["dres"], L["dw"], wl.eps, L["outs"][1], L["outs"][2])
-            for ho, o in zip(L["houts"], L["outs"]):
-                ho.copy_(o, non_blocking=True)
+            L["hout"].copy_(L["dout"], non_blocking=True)
 
     for i in range(warmup):
         step(i)
@@ -375,9 +386,7 @@ def e2e(arm, wl, steps, warmup, streams=1):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     c.close()
-    h2d = sum(x.numel() * x.element_size() for x in hx) + hres.numel() * hres.element_size() + hw.numel() * hw.element_size()
-    d2h = sum(o.numel() * o.element_size() for o in lanes[0]["houts"])
-    return ms, h2d, d2h
+    return ms, total, 3 * D
 
 
 def latency_row(arm, wl, outputs, calls=12000):
