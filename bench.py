@@ -395,7 +395,7 @@ def latency_row(arm, wl, outputs, calls=12000):
     2x L2 when that fits in `calls`, so most reads come from HBM)."""
     torch, car = arm.torch, arm.car
     set_bytes = bytes_fused(wl, outputs)
-    n = min(calls, max(64, -(-2 * L2_BYTES // set_bytes)))
+    n = min(calls, max(64, 2 * L2_BYTES // set_bytes + 1))
     sets = make_sets(torch, wl, arm.dev, n, outputs=("ar", "ro", "no"))
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
     lib, h = arm.lib, c.h

@@ -310,7 +310,7 @@ const char* car_last_error(void);
  * CTA whole rows, 2 splits every row over a CTA pair (needs an even number of
  * 16-byte columns); threads and vpt must be 0; needs N*s <= 100 KiB per CTA.
  * CAR_FUSED_AUTO (all fields 0) restores the automatic choice: the pipeline
- * with whole rows when M >= 1.5 x the SM count, else rows (one CTA per row,
+ * with whole rows when M exceeds the SM count, else rows (one CTA per row,
  * or eight per row for a few rows wider than 512 16-byte vectors).
  * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_SIZE when the shape
  * does not cover a row or the row does not fit the ring. */

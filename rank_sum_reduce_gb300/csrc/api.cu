@@ -162,13 +162,13 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
   return (int64_t)sh.threads * sh.vpt >= chunk;
 }
 
-// The pipelined kernel is faster once every SM has one and a half rows to
-// stream.  Measured on GB300 against the row kernel with one CTA per row:
-// W = 8 N = 8192 bf16 at M = 152, 6.5 (rows) against 7.4 us (pipeline); at
-// M = 200 mixed (W = 8: 9.5 against 9.8, W = 4: 7.3 against 7.1); from M = 228
-// the pipeline wins (W = 8: 10.0 against 10.3, M = 456: 14.6 against 16.9).
+// The pipelined kernel is faster once there are more rows than SMs.  Measured
+// on GB300 against the row kernel (both fetching their first row into L2
+// before the PDL wait), N = 8192 bf16: at M = 152, W = 8 5.8 (rows) against
+// 6.5 us (pipeline), W = 2 3.3 against 3.8; at M = 184, W = 8 8.2 against
+// 7.5, W = 2 5.3 against 4.5; at M = 456, W = 8 15.4 against 13.4.
 int auto_fused_kernel(const car_ctx* h) {
-  return (h->tma_ok && 2 * h->M >= 3 * (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
+  return (h->tma_ok && h->M > (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
 }
 
 // Row-kernel shape for the Lamport receive step: the same rules as the fused

@@ -165,6 +165,14 @@ __device__ __forceinline__ void rank_sum(const uint4 (&raw)[W], int n, float (&a
 // the resident CTA count, so the early trigger cannot keep this grid's own
 // CTAs from being scheduled.
 // ---------------------------------------------------------------------------
+// Ask L2 (not L1) for `bytes` bytes at `p`: 16-byte aligned, a multiple of 16
+// bytes.  L2 is coherent for the whole GPU, so this may run before
+// griddepcontrol.wait: a load after the wait still sees every write the grid
+// it waits for makes, and only the HBM latency moves ahead of the wait.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -69,6 +69,18 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int col0 = crank * p.chunk;
   int parity = 0;
+  // While the previous grid of the stream finishes: this CTA's slice of its
+  // first row (W ranks, residual, weight) into L2, one bulk prefetch per slice.
+  {
+    const int64_t row0 = blockIdx.x / C;
+    const int nvec = min(p.chunk, p.vec_per_row - col0);
+    if (row0 < p.rows && nvec > 0 && (int)threadIdx.x < n + 2) {
+      const int64_t off = row0 * (int64_t)p.vec_per_row + col0;
+      const int t = threadIdx.x;
+      const uint4* src = t < n ? static_cast<const uint4*>(p.in.p[t]) + off : (t == n ? p.residual + off : p.weight + col0);
+      prefetch_l2(src, (uint32_t)nvec * 16u);
+    }
+  }
   pdl_wait_and_release();
 
   for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups) {

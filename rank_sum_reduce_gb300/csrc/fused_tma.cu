@@ -417,6 +417,16 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
   }
   __syncthreads();
   if (C > 1) cluster_barrier();  // peers' barriers exist before anyone arrives on them
+  // While the previous grid of the stream finishes: this CTA's piece of its
+  // first row (W ranks, residual, weight) into L2, one bulk prefetch each.
+  if (group < p.rows && (int)threadIdx.x < n + 2) {
+    const int t = threadIdx.x;
+    const int64_t off = group * (int64_t)p.row_bytes + (int64_t)crank * slice;
+    const void* src = t < n    ? static_cast<const void*>(static_cast<const uint8_t*>(p.in.p[t]) + off)
+                      : t == n ? static_cast<const void*>(p.residual + off)
+                               : static_cast<const void*>(p.weight + (int64_t)crank * cols);
+    prefetch_l2(src, (uint32_t)slice);
+  }
   pdl_wait_and_release();        // inputs may come from the previous kernel of the stream
 
   if (warp == nconsumer_warps) {
