@@ -577,7 +577,10 @@ def ll128_row(arm, iters=10):
     xs = [workloads.make_x(wl, r, arm.dev) for r in range(wl.W)]
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
     wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(wl.W)]
-    enc_ms = timed(torch, lambda i: [c.ll128_encode(x, wl.ll128_flag, wv) for x, wv in zip(xs, wires)], 3) / wl.W
+    g = capture(torch, [(lambda x, wv: (lambda s: c.ll128_encode(x, wl.ll128_flag, wv, stream=s)))(x, wv)
+                        for x, wv in zip(xs, wires)])
+    enc_ms = timed(torch, lambda i: g.replay(), 3) / wl.W
+    del g
     stale = workloads.stale_lines(L, wl.W, wl.seed, wl.ll128_stale_every)
     old = torch.tensor(list(wl.ll128_stale_flag.to_bytes(8, "little")), dtype=torch.uint8, device=arm.dev)
     for wv, idx in zip(wires, stale):
@@ -671,14 +674,18 @@ def ll128_misaligned_row(arm, M, launches, reps=5):
 
 
 def ll_row(arm, iters=20):
-    """LL encode + validate/decode/reduce at the headline shape (W=8, 8 MB per rank)."""
+    """LL encode + validate/decode/reduce at the headline shape (W=8, 8 MB per rank);
+    encode time per call from graph replay of 64 calls over the 8 ranks."""
     torch, car = arm.torch, arm.car
     wl = workloads.WORKLOADS[HEADLINE]
     D = wl.data_bytes
     xs = [workloads.make_x(wl, r, arm.dev) for r in range(wl.W)]
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
     wires = [torch.empty(c.ll_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(wl.W)]
-    enc_ms = timed(torch, lambda i: [c.ll_encode(x, 7, wv) for x, wv in zip(xs, wires)], 5) / wl.W
+    g = capture(torch, [(lambda x, wv: (lambda s: c.ll_encode(x, 7, wv, stream=s)))(xs[i % wl.W], wires[i % wl.W])
+                        for i in range(8 * wl.W)])
+    enc_ms = timed(torch, lambda i: g.replay(), 5) / (8 * wl.W)
+    del g
     out = torch.empty_like(xs[0])
     dec_ms = timed(torch, lambda i: c.ll_decode_reduce(wires, 7, out), iters)
     n_stale, _ = c.ll_report()

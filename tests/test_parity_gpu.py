@@ -393,6 +393,8 @@ WIRE_CASES = [
     # (W, M, N, dtype): lines odd/even, partial last line, single line, many pairs
     (2, 1, 8, "bf16"), (3, 1, 56, "bf16"), (2, 1, 64, "bf16"), (4, 3, 1000, "bf16"), (16, 5, 776, "bf16"),
     (5, 7, 1544, "fp16"), (8, 9, 1020, "fp32"), (1, 1, 120, "bf16"), (2, 2, 60, "fp32"), (8, 31, 4096, "bf16"),
+    # 8 MiB per rank: more warps of work than the resident grid, so the grid-stride loops wrap
+    (2, 1024, 4096, "bf16"),
 ]
 
 
