@@ -21,20 +21,22 @@
 namespace car {
 namespace {
 
-template <int DT, int W, int U>
-__global__ void __launch_bounds__(kReduceThreads)
-    rank_sum_reduce_kernel(const RankPtrs in, const int nranks, uint4* __restrict__ out,
-                           const int64_t nvec) {
-  constexpr int R = W > 0 ? W : kMaxRanks;
-  const int n = W > 0 ? W : nranks;
-  // this CTA's share [lo, hi): nvec / grid vectors, one more for the first nvec % grid CTAs
+// This CTA's share [lo, hi) of the vectors: nvec / grid, one more for the
+// first nvec % grid CTAs.
+__device__ __forceinline__ void cta_share(const int64_t nvec, int64_t* lo, int64_t* hi) {
   const int64_t share = nvec / gridDim.x, extra = nvec % gridDim.x;
-  const int64_t lo = share * blockIdx.x + (blockIdx.x < extra ? blockIdx.x : extra);
-  const int64_t hi = lo + share + (blockIdx.x < extra ? 1 : 0);
-  // While the previous grid of the stream finishes: the first pass of the
-  // share into L2, one request per 128-byte line (a line's first vector, and
-  // the pass's first vector).  Per-thread requests, not bulk ones: a bulk
-  // prefetch per rank measured slower, alone and after the fused kernel.
+  *lo = share * blockIdx.x + (blockIdx.x < extra ? blockIdx.x : extra);
+  *hi = *lo + share + (blockIdx.x < extra ? 1 : 0);
+}
+
+// Called before the PDL wait, while the previous grid of the stream
+// finishes: the first pass (kReduceThreads * U vectors) of the share, every
+// rank, into L2, one request per 128-byte line (a line's first vector, and
+// the pass's first vector).  Per-thread requests, not bulk ones: a bulk
+// prefetch per rank measured slower, alone and after the fused kernel.
+template <int R, int U>
+__device__ __forceinline__ void prefetch_first_pass(const RankPtrs& in, const int n, const int64_t lo,
+                                                    const int64_t hi) {
 #pragma unroll
   for (int u = 0; u < U; u++) {
     const int64_t v = lo + threadIdx.x + (int64_t)u * kReduceThreads;
@@ -46,6 +48,17 @@ __global__ void __launch_bounds__(kReduceThreads)
       }
     }
   }
+}
+
+template <int DT, int W, int U>
+__global__ void __launch_bounds__(kReduceThreads)
+    rank_sum_reduce_kernel(const RankPtrs in, const int nranks, uint4* __restrict__ out,
+                           const int64_t nvec) {
+  constexpr int R = W > 0 ? W : kMaxRanks;
+  const int n = W > 0 ? W : nranks;
+  int64_t lo, hi;
+  cta_share(nvec, &lo, &hi);
+  prefetch_first_pass<R, U>(in, n, lo, hi);
   pdl_wait_and_release();
   for (int64_t base = lo + threadIdx.x; base < hi; base += kReduceThreads * U) {
     uint4 raw[U][R];
@@ -88,15 +101,16 @@ __global__ void __launch_bounds__(kReduceThreads)
     for (int r = 0; r < kMaxRanks; r++) s_ptr[r] = static_cast<const uint4*>(in.p[r]);
   }
   __syncthreads();
+  int64_t lo, hi;
+  cta_share(nvec, &lo, &hi);
+  prefetch_first_pass<R, U>(in, n, lo, hi);
   pdl_wait_and_release();
-  const int64_t step = (int64_t)gridDim.x * kReduceThreads * U;
-  for (int64_t base = (int64_t)blockIdx.x * kReduceThreads * U + threadIdx.x; base < nvec;
-       base += step) {
+  for (int64_t base = lo + threadIdx.x; base < hi; base += kReduceThreads * U) {
     uint4 raw[U][R];
 #pragma unroll
     for (int u = 0; u < U; u++) {
       const int64_t v = base + (int64_t)u * kReduceThreads;
-      if (v < nvec) {
+      if (v < hi) {
         int owner = n - 1;
         if (part > 0 && v / part < n - 1) owner = (int)(v / part);
 #pragma unroll
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(kReduceThreads)
 #pragma unroll
     for (int u = 0; u < U; u++) {
       const int64_t v = base + (int64_t)u * kReduceThreads;
-      if (v < nvec) {
+      if (v < hi) {
         float acc[Pack<DT>::kN];
         rank_sum<DT, R>(raw[u], n, acc);
         st16(out + v, Pack<DT>::narrow(acc));
