@@ -590,6 +590,33 @@ def test_chained_calls_see_previous_outputs(car, M):
         ref_res, ref_x0 = ref_ro, ref_ar
 
 
+@pytest.mark.parametrize("kind", ["one_shot", "two_shot"])
+@pytest.mark.parametrize("W,M,N", [(4, 33, 1032), (8, 512, 8192)])
+def test_chained_reduces_see_previous_output(car, kind, W, M, N):
+    """Back-to-back reduces where call k's rank-0 input is call k-1's output:
+    each call's L2 prefetch runs before it waits for its predecessor, and
+    every call must still read the predecessor's result."""
+    steps = 4
+    wl = workloads.custom(W, M, N, "bf16", seed=950 + W + M)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    dx = [x.to(DEV) for x in xs]
+    outs = [torch.full_like(dx[0], float("nan")) for _ in range(steps)]
+    with car.Car(W, M, N, "bf16") as c:
+        run = c.reduce if kind == "one_shot" else c.reduce_two_shot
+        cur = dx[0]
+        for k in range(steps):
+            run([cur] + dx[1:], outs[k])
+            cur = outs[k]
+        c.sync()
+    torch.cuda.synchronize()
+    ref = xs[0]
+    for k in range(steps):
+        want = torch.empty_like(xs[0])
+        (oracle.reduce if kind == "one_shot" else oracle.reduce_two_shot)([ref] + xs[1:], "bf16", want)
+        assert_bits_equal(outs[k], want, f"{kind} step {k}")
+        ref = want
+
+
 @pytest.mark.parametrize("M", [1, 400])
 def test_graph_capture_replays_correctly(car, M):
     """Capture reduce + fused + LL128 encode/decode in one CUDA graph, change
