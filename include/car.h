@@ -310,8 +310,10 @@ const char* car_last_error(void);
  * CTA whole rows, 2 splits every row over a CTA pair (needs an even number of
  * 16-byte columns); threads and vpt must be 0; needs N*s <= 100 KiB per CTA.
  * CAR_FUSED_AUTO (all fields 0) restores the automatic choice: the pipeline
- * with whole rows when M exceeds the SM count, else rows (one CTA per row,
- * or eight per row for a few rows wider than 512 16-byte vectors).
+ * with whole rows when M exceeds the SM count, else rows: a row split over a
+ * cluster of 8 or 4 CTAs while each CTA keeps at least 128 16-byte vectors,
+ * the CTAs fit in 7/8 of the SMs, and M <= 16 or a row brings at least 48 KB
+ * of inputs; one CTA per row otherwise.
  * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_SIZE when the shape
  * does not cover a row or the row does not fit the ring. */
 car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int vpt);

@@ -125,25 +125,33 @@ int clamp_grid(int64_t needed, int per_sm, int num_sms) {
 
 int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
 
-// Automatic shape of the row-split fused kernel.
-//  * Many rows (M >= 2 x SMs): one CTA per row, the fewest vectors per
-//    thread that the compiled instances allow; split the row over a cluster
-//    only when a single CTA cannot cover it.
-//  * Few rows: split a row over a cluster only while each CTA still pulls
-//    more than about 24 KB of inputs and the SMs are not yet all busy; a
-//    cluster barrier costs about 0.4 us, which a small row cannot repay
-//    (measured on GB300: W=2, N=2048 bf16 runs best on one CTA, W=8,
-//    N=8192 bf16 on eight).
+// Automatic shape of the row-split fused kernel.  A row is split over a
+// cluster of c = 8 or 4 CTAs (the largest that qualifies) when
+//  * each CTA keeps at least 128 16-byte vectors of the row,
+//  * the c * M CTAs stay within 7/8 of the SMs (one wave of clusters), and
+//  * there are at most 16 rows, or each row brings at least 48 KB of inputs;
+// otherwise one CTA takes a row, with the fewest vectors per thread that the
+// compiled instances allow.  A row too wide for one CTA's threads takes the
+// smallest cluster whose CTAs cover it.
 car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
-  // Measured on GB300 (bf16, W = 2..16, M = 1..128, N = 2048..8192): a
-  // cluster of two never paid for its barrier.  A few wide rows (more than
-  // 512 vectors, 8 M <= SMs) ran fastest split over eight CTAs (W = 2, M = 1,
-  // N = 8192: 2.64 against 2.90 us with two; W = 8, M = 8, N = 8192: 3.04
-  // against 3.48 us with one), every other shape with one CTA per row and one
-  // or two vectors per thread (W = 8, M = 128, N = 8192: 6.00 against 8.25 us
-  // with two CTAs per row).  A row too wide for one CTA's threads takes the
-  // smallest cluster whose CTAs cover it.
-  for (int c = (V > 512 && 8 * M <= num_sms) ? 8 : 1; c <= 8; c *= 2) {
+  // Measured on GB300 with the partials pushed by st.async (graph replay over
+  // cold inputs, bf16 unless noted; us per call, rule's choice against one CTA
+  // per row): W = 8, N = 8192: M = 1 1.97 / 3.01, M = 32 (c = 4) 2.70 / 3.19;
+  // W = 8, N = 4096, M = 1 (c = 4) 1.90 / 2.19; W = 2, N = 8192, M = 32
+  // (c = 4) 2.26 / 2.45.  Where the rule keeps one CTA per row it was as fast
+  // or faster: W = 4, N = 4096, M = 32: 2.09 against 2.20 with four CTAs;
+  // W = 2, N = 2048, M = 1: 1.48 against 1.64 with two.
+  const int64_t row_in = (int64_t)(W + 1) * V * 16;
+  for (int c = 8; c >= 4; c /= 2) {
+    if (V / c < 128 || (int64_t)c * M > num_sms - num_sms / 8 || (M > 16 && row_in < 48 * 1024)) continue;
+    const int chunk = (V + c - 1) / c;
+    for (int vpt = 1; vpt <= 2; vpt++) {
+      if (!car::fused_has_variant(W, vpt)) continue;
+      const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
+      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{c, t, vpt, 1};
+    }
+  }
+  for (int c = 1; c <= 8; c *= 2) {
     const int chunk = (V + c - 1) / c;
     for (int vpt = 1; vpt <= 2; vpt++) {
       if (!car::fused_has_variant(W, vpt)) continue;
@@ -474,8 +482,8 @@ car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, co
     e = car::launch_fused_tma(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out,
                               h->d_err, h->M, h->N, h->vec_per_row, h->tma, static_cast<cudaStream_t>(stream));
   else
-    e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out, h->M,
-                          h->N, h->vec_per_row, h->fused, static_cast<cudaStream_t>(stream));
+    e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out, h->d_err,
+                          h->M, h->N, h->vec_per_row, h->fused, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "reduce_residual_rmsnorm launch");
 }
 

@@ -38,7 +38,7 @@ bool fused_has_variant(int W, int vpt);
 cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int num_sms, int* groups);
 cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
                          const void* weight, float eps, void* residual_out, void* norm_out,
-                         void* ar_out, int64_t rows, int64_t cols, int vec_per_row,
+                         void* ar_out, unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
                          const FusedShape& sh, cudaStream_t s);
 
 // ---- fused, many rows: TMA bulk copies into a shared-memory ring (fused_tma.cu) ----

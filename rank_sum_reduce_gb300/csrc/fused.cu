@@ -16,12 +16,8 @@
 // takes a row and CTAs loop over rows (grid capped at the resident count).
 // h never leaves registers.  Roofline: HBM, (W + 1 + outputs) * 16 bytes per
 // vector plus the weight row.
-#include <cooperative_groups.h>
-
 #include "car_device.cuh"
 #include "car_launch.h"
-
-namespace cg = cooperative_groups;
 
 namespace car {
 namespace {
@@ -33,6 +29,7 @@ struct FusedParams {
   uint4* residual_out;
   uint4* norm_out;
   uint4* ar_out;  // may be null
+  unsigned int* err;  // bit 0: a CTA gave up waiting for its cluster peers' partials
   float eps;
   float cols;     // N, exactly representable (N <= 2^24)
   int64_t rows;
@@ -60,15 +57,26 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : p.nranks;
   __shared__ float s_warp[32];
-  __shared__ float s_part[2];  // this CTA's partial, double-buffered by row parity
+  __shared__ float s_part[2][8];               // the cluster's CTA partials, by row parity
+  __shared__ __align__(8) uint64_t s_xbar[2];  // all C partials of the row have landed, by row parity
   __shared__ float s_total;
 
   const int C = p.cluster;
-  const int crank = C > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int crank = C > 1 ? (int)cluster_rank() : 0;
   const int64_t ngroups = gridDim.x / C;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int col0 = crank * p.chunk;
-  int parity = 0;
+  uint32_t it = 0;  // rows done by this CTA
+  bool peers_ready = C == 1;
+  if (C > 1) {
+    if (threadIdx.x == 0) {
+      mbar_init(&s_xbar[0], 1);  // each phase: the local expect_tx arrive plus C x 4 bytes
+      mbar_init(&s_xbar[1], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_arrive();  // its wait, before the first partial is sent, covers the loads
+  }
   // While the previous grid of the stream finishes: this CTA's slice of its
   // first row (W ranks, residual, weight) into L2, one bulk prefetch per slice.
   {
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   }
   pdl_wait_and_release();
 
-  for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups) {
+  for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups, it++) {
     const int64_t rbase = row * (int64_t)p.vec_per_row;
 
     // 1. all loads of this thread's vectors: W ranks + residual
@@ -126,29 +134,36 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
     }
 
     // 3. row statistic: warp shuffle, then shared memory across warps, then
-    //    (split rows) distributed shared memory across the cluster.  Every CTA
-    //    of a row adds the same partials in the same order, so all of them see
-    //    the same total.
+    //    (split rows) each CTA pushes its partial into every CTA of the
+    //    cluster (st.async, counted on the receiver's mbarrier) and adds the
+    //    C partials in rank order once they have landed: one one-way hop, and
+    //    every CTA of the row sees the same total.
     ss = warp_sum(ss);
     if (lane == 0) s_warp[warp] = ss;
+    if (!peers_ready) {
+      cluster_wait();  // every peer's mbarriers are initialised
+      peers_ready = true;
+    }
     __syncthreads();
     if (warp == 0) {
       float t = lane < nwarps ? s_warp[lane] : 0.f;
       t = warp_sum(t);
       if (lane == 0) {
-        if (C > 1) s_part[parity] = t;
-        else s_total = t;
+        if (C > 1) {
+          const uint32_t b = it & 1u;
+          mbar_arrive_expect_tx(&s_xbar[b], 4u * (uint32_t)C);
+          for (int r = 0; r < C; r++)
+            st_async_f32(map_rank(&s_part[b][crank], (uint32_t)r), t, map_rank(&s_xbar[b], (uint32_t)r));
+          if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
+            t = s_part[b][0];
+            for (int r = 1; r < C; r++) t += s_part[b][r];
+          } else {
+            atomicOr(p.err, 1u);
+            t = __int_as_float(0x7fc00000);  // NaN: this row's norm_out is not usable
+          }
+        }
+        s_total = t;
       }
-    }
-    if (C > 1) {
-      cg::cluster_group cluster = cg::this_cluster();
-      cluster.sync();
-      if (warp == 0) {
-        float t = lane < C ? *cluster.map_shared_rank(&s_part[parity], lane) : 0.f;
-        t = warp_sum(t);
-        if (lane == 0) s_total = t;
-      }
-      parity ^= 1;
     }
     __syncthreads();
     const float rms = rsqrtf(__fdiv_rn(s_total, p.cols) + p.eps);
@@ -167,8 +182,10 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       }
     }
   }
-  // A CTA's partial may still be read by its peers: leave together.
-  if (C > 1) cg::this_cluster().sync();
+  // Nothing reaches this CTA's shared memory after its last row's wait (each
+  // peer sends one partial per row), so no exit barrier is needed; a cluster
+  // with no row still pairs its first arrive.
+  if (!peers_ready) cluster_wait();
 }
 
 using FusedFn = void (*)(const FusedParams);
@@ -256,7 +273,7 @@ cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int nu
 
 cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
                          const void* weight, float eps, void* residual_out, void* norm_out,
-                         void* ar_out, int64_t rows, int64_t cols, int vec_per_row,
+                         void* ar_out, unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
                          const FusedShape& sh, cudaStream_t s) {
   FusedFn fn = pick_fused(dtype, W, sh.vpt);
   if (!fn) return cudaErrorInvalidValue;
@@ -267,6 +284,7 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
   p.residual_out = static_cast<uint4*>(residual_out);
   p.norm_out = static_cast<uint4*>(norm_out);
   p.ar_out = static_cast<uint4*>(ar_out);
+  p.err = err;
   p.eps = eps;
   p.cols = (float)cols;
   p.rows = rows;
