@@ -125,41 +125,52 @@ int clamp_grid(int64_t needed, int per_sm, int num_sms) {
 
 int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
 
-// Automatic shape of the row-split fused kernel.  A row is split over a
-// cluster of c = 8 or 4 CTAs (the largest that qualifies) when
+// Automatic shape of a row-split kernel (the fused row kernel and the Lamport
+// receive), given which (W, vectors per thread) instances are compiled and
+// their thread limits.  A row is split over a cluster of c = 8 or 4 CTAs (the
+// largest that qualifies) when
 //  * each CTA keeps at least 128 16-byte vectors of the row,
 //  * the c * M CTAs stay within 7/8 of the SMs (one wave of clusters), and
 //  * there are at most 16 rows, or each row brings at least 48 KB of inputs;
 // otherwise one CTA takes a row, with the fewest vectors per thread that the
 // compiled instances allow.  A row too wide for one CTA's threads takes the
 // smallest cluster whose CTAs cover it.
-car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
-  // Measured on GB300 with the partials pushed by st.async (graph replay over
-  // cold inputs, bf16 unless noted; us per call, rule's choice against one CTA
-  // per row): W = 8, N = 8192: M = 1 1.97 / 3.01, M = 32 (c = 4) 2.70 / 3.19;
-  // W = 8, N = 4096, M = 1 (c = 4) 1.90 / 2.19; W = 2, N = 8192, M = 32
-  // (c = 4) 2.26 / 2.45.  Where the rule keeps one CTA per row it was as fast
-  // or faster: W = 4, N = 4096, M = 32: 2.09 against 2.20 with four CTAs;
-  // W = 2, N = 2048, M = 1: 1.48 against 1.64 with two.
+//
+// Measured on GB300 for the fused row kernel, with the partials pushed by
+// st.async (graph replay over cold inputs, bf16; us per call, rule's choice
+// against one CTA per row): W = 8, N = 8192: M = 1 1.97 / 3.01, M = 32
+// (c = 4) 2.70 / 3.19; W = 8, N = 4096, M = 1 (c = 4) 1.90 / 2.19; W = 2,
+// N = 8192, M = 32 (c = 4) 2.26 / 2.45.  Where the rule keeps one CTA per row
+// it was as fast or faster: W = 4, N = 4096, M = 32: 2.09 against 2.20 with
+// four CTAs; W = 2, N = 2048, M = 1: 1.48 against 1.64 with two.
+template <class HasVariant, class MaxThreads>
+car::FusedShape row_split_shape(int W, int64_t M, int V, int num_sms, HasVariant has_variant,
+                                MaxThreads max_threads) {
+  auto fit = [&](int c, car::FusedShape* out) {
+    const int chunk = (V + c - 1) / c;
+    for (int vpt = 1; vpt <= 2; vpt++) {
+      if (!has_variant(W, vpt)) continue;
+      const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
+      if (t <= max_threads(W, vpt)) {
+        *out = car::FusedShape{c, t, vpt, 1};
+        return true;
+      }
+    }
+    return false;
+  };
+  car::FusedShape sh;
   const int64_t row_in = (int64_t)(W + 1) * V * 16;
   for (int c = 8; c >= 4; c /= 2) {
     if (V / c < 128 || (int64_t)c * M > num_sms - num_sms / 8 || (M > 16 && row_in < 48 * 1024)) continue;
-    const int chunk = (V + c - 1) / c;
-    for (int vpt = 1; vpt <= 2; vpt++) {
-      if (!car::fused_has_variant(W, vpt)) continue;
-      const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
-      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{c, t, vpt, 1};
-    }
+    if (fit(c, &sh)) return sh;
   }
-  for (int c = 1; c <= 8; c *= 2) {
-    const int chunk = (V + c - 1) / c;
-    for (int vpt = 1; vpt <= 2; vpt++) {
-      if (!car::fused_has_variant(W, vpt)) continue;
-      const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
-      if (t <= car::fused_max_threads(W, vpt)) return car::FusedShape{c, t, vpt, 1};
-    }
-  }
+  for (int c = 1; c <= 8; c *= 2)
+    if (fit(c, &sh)) return sh;
   return car::FusedShape{8, std::max(32, round_up32((V + 7) / 8)), 1, 1};  // rows past CAR_MAX_ROW_BYTES only
+}
+
+car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
+  return row_split_shape(W, M, V, num_sms, car::fused_has_variant, car::fused_max_threads);
 }
 
 bool shape_valid(int W, int V, const car::FusedShape& sh) {
@@ -180,22 +191,9 @@ int auto_fused_kernel(const car_ctx* h) {
 }
 
 // Row-kernel shape for the Lamport receive step: the same rules as the fused
-// row-split kernel, within the Lamport kernel's compiled instances.
+// row kernel, within the Lamport kernel's compiled instances.
 car::FusedShape auto_lamport_shape(int W, int64_t M, int V, int num_sms) {
-  if (M >= 2 * (int64_t)num_sms) {
-    for (int vpt = 1; vpt <= 2; vpt++) {
-      if (!car::lamport_has_variant(W, vpt)) continue;
-      const int t = round_up32((V + vpt - 1) / vpt);
-      if (t <= car::lamport_max_threads(W, vpt)) return car::FusedShape{1, t, vpt, 1};
-    }
-  }
-  int c = 1;
-  if (M < 2 * (int64_t)num_sms) {
-    const int64_t row_input_bytes = (int64_t)(W + 1) * V * 16;
-    while (c < 8 && row_input_bytes / c > 24 * 1024 && (int64_t)c * M < num_sms) c *= 2;
-  }
-  while (c < 8 && (V + c - 1) / c > car::lamport_max_threads(W, 1)) c *= 2;
-  return car::FusedShape{c, std::max(32, round_up32((V + c - 1) / c)), 1, 1};
+  return row_split_shape(W, M, V, num_sms, car::lamport_has_variant, car::lamport_max_threads);
 }
 
 car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
@@ -589,8 +587,8 @@ car_status car_lamport_reduce_residual_rmsnorm(car_ctx* h, void* comm, uint64_t 
   uint8_t* base = static_cast<uint8_t*>(comm);
   e = car::launch_lamport_reduce(h->W, base + (int64_t)(round % 3) * region_bytes,
                                  base + (int64_t)((round + 2) % 3) * region_bytes, h->D, residual, weight, eps,
-                                 residual_out, norm_out, ar_out, h->log[2], next_log_slot(h, 2), max_polls, h->M,
-                                 h->N, h->vec_per_row, h->lamport, s);
+                                 residual_out, norm_out, ar_out, h->log[2], next_log_slot(h, 2), max_polls,
+                                 h->d_err, h->M, h->N, h->vec_per_row, h->lamport, s);
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "lamport receive launch");
 }
 

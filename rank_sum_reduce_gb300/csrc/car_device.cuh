@@ -214,6 +214,12 @@ __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t ba
                "r"(bar)
                : "memory");
 }
+// The same for two 32-bit words (8 bytes, `addr` 8-byte aligned).
+__device__ __forceinline__ void st_async_v2_b32(uint32_t addr, uint32_t x, uint32_t y, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "r"(x), "r"(y), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

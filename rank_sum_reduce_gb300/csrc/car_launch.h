@@ -78,8 +78,8 @@ cudaError_t launch_lamport_push(const void* data, int64_t bytes, void* slot, int
 cudaError_t launch_lamport_reduce(int W, const void* region, void* clear_region, int64_t slot_bytes,
                                   const void* residual, const void* weight, float eps, void* residual_out,
                                   void* norm_out, void* ar_out, StaleLog* log, int log_slot, int max_polls,
-                                  int64_t rows,
-                                  int64_t cols, int vec_per_row, const FusedShape& sh, cudaStream_t s);
+                                  unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
+                                  const FusedShape& sh, cudaStream_t s);
 
 // ---- diagnostics (api.cu): text returned by car_last_error() on this thread ----
 void set_last_error(const char* msg);

@@ -18,12 +18,8 @@
 // are 0 and each (rank, row) is logged.  Roofline: HBM; a row reads
 // W + 1 row slices and the weight, writes 2-3 output rows and W sentinel
 // rows.
-#include <cooperative_groups.h>
-
 #include "car_device.cuh"
 #include "car_launch.h"
-
-namespace cg = cooperative_groups;
 
 namespace car {
 namespace {
@@ -65,6 +61,7 @@ struct LamportParams {
   uint4* ar_out;             // may be null
   StaleLog* log;
   int log_slot;
+  unsigned int* err;         // bit 0: a CTA gave up waiting for its cluster peers' partials
   float eps;
   float cols;
   int64_t rows;
@@ -94,21 +91,31 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   const int n = W > 0 ? W : p.nranks;
   __shared__ float s_warp[32];
   __shared__ uint32_t s_miss_warp[32];
-  __shared__ float s_part[2];
-  __shared__ uint32_t s_miss_part[2];
+  __shared__ __align__(8) uint2 s_part[2][8];  // the cluster's CTA (partial, mask) pairs, by row parity
+  __shared__ __align__(8) uint64_t s_xbar[2];  // all C pairs of the row have landed, by row parity
   __shared__ float s_total;
   __shared__ uint32_t s_miss;
 
   const int C = p.cluster;
-  const int crank = C > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int crank = C > 1 ? (int)cluster_rank() : 0;
   const int64_t ngroups = gridDim.x / C;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int col0 = crank * p.chunk;
-  int parity = 0;
+  uint32_t it = 0;  // rows done by this CTA
+  bool peers_ready = C == 1;
+  if (C > 1) {
+    if (threadIdx.x == 0) {
+      mbar_init(&s_xbar[0], 1);  // each phase: the local expect_tx arrive plus C x 8 bytes
+      mbar_init(&s_xbar[1], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_arrive();  // its wait, before the first pair is sent, covers the loads
+  }
   pdl_wait_and_release();
   prepare_next_log(p.log, p.log_slot);
 
-  for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups) {
+  for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups, it++) {
     const int64_t rbase = row * (int64_t)p.vec_per_row;
     uint4 raw[VPT][R];
     uint4 res[VPT], wv[VPT];
@@ -169,12 +176,19 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       }
     }
 
-    // row statistic and row "missing" mask: warp -> CTA -> cluster
+    // row statistic and row "missing" mask: warp -> CTA -> cluster.  Split
+    // rows: each CTA pushes its (partial, mask) pair into every CTA of the
+    // cluster with st.async and combines the C pairs in rank order once they
+    // have landed, so every CTA of the row sees the same total and mask.
     ss = warp_sum(ss);
     miss = __reduce_or_sync(0xFFFFFFFFu, miss);
     if (lane == 0) {
       s_warp[warp] = ss;
       s_miss_warp[warp] = miss;
+    }
+    if (!peers_ready) {
+      cluster_wait();  // every peer's mbarriers are initialised
+      peers_ready = true;
     }
     __syncthreads();
     if (warp == 0) {
@@ -184,28 +198,26 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       m = __reduce_or_sync(0xFFFFFFFFu, m);
       if (lane == 0) {
         if (C > 1) {
-          s_part[parity] = t;
-          s_miss_part[parity] = m;
-        } else {
-          s_total = t;
-          s_miss = m;
+          const uint32_t b = it & 1u;
+          mbar_arrive_expect_tx(&s_xbar[b], 8u * (uint32_t)C);
+          for (int r = 0; r < C; r++)
+            st_async_v2_b32(map_rank(&s_part[b][crank], (uint32_t)r), __float_as_uint(t), m,
+                            map_rank(&s_xbar[b], (uint32_t)r));
+          if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
+            t = __uint_as_float(s_part[b][0].x);
+            m = s_part[b][0].y;
+            for (int r = 1; r < C; r++) {
+              t += __uint_as_float(s_part[b][r].x);
+              m |= s_part[b][r].y;
+            }
+          } else {
+            atomicOr(p.err, 1u);
+            m = (1u << n) - 1u;  // the row's outputs are zeroed and every rank is logged for it
+          }
         }
+        s_total = t;
+        s_miss = m;
       }
-    }
-    if (C > 1) {
-      cg::cluster_group cluster = cg::this_cluster();
-      cluster.sync();
-      if (warp == 0) {
-        float t = lane < C ? *cluster.map_shared_rank(&s_part[parity], lane) : 0.f;
-        uint32_t m = lane < C ? *cluster.map_shared_rank(&s_miss_part[parity], lane) : 0u;
-        t = warp_sum(t);
-        m = __reduce_or_sync(0xFFFFFFFFu, m);
-        if (lane == 0) {
-          s_total = t;
-          s_miss = m;
-        }
-      }
-      parity ^= 1;
     }
     __syncthreads();
     const uint32_t row_miss = s_miss;
@@ -238,7 +250,10 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       }
     }
   }
-  if (C > 1) cg::this_cluster().sync();
+  // Nothing reaches this CTA's shared memory after its last row's wait (each
+  // peer sends one pair per row), so no exit barrier is needed; a cluster with
+  // no row still pairs its first arrive.
+  if (!peers_ready) cluster_wait();
 }
 
 using LamportFn = void (*)(const LamportParams);
@@ -309,8 +324,8 @@ cudaError_t launch_lamport_push(const void* data, int64_t bytes, void* slot, int
 cudaError_t launch_lamport_reduce(int W, const void* region, void* clear_region, int64_t slot_bytes,
                                   const void* residual, const void* weight, float eps, void* residual_out,
                                   void* norm_out, void* ar_out, StaleLog* log, int log_slot, int max_polls,
-                                  int64_t rows,
-                                  int64_t cols, int vec_per_row, const FusedShape& sh, cudaStream_t s) {
+                                  unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
+                                  const FusedShape& sh, cudaStream_t s) {
   LamportFn fn = pick_lamport(W, sh.vpt);
   if (!fn) return cudaErrorInvalidValue;
   LamportParams p;
@@ -324,6 +339,7 @@ cudaError_t launch_lamport_reduce(int W, const void* region, void* clear_region,
   p.ar_out = static_cast<uint4*>(ar_out);
   p.log = log;
   p.log_slot = log_slot;
+  p.err = err;
   p.eps = eps;
   p.cols = (float)cols;
   p.rows = rows;
