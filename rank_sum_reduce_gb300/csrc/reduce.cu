@@ -138,11 +138,15 @@ __global__ void __launch_bounds__(kReduceThreads)
 using ReduceFn = void (*)(const RankPtrs, const int, uint4*, const int64_t);
 using TwoShotFn = void (*)(const RankPtrs, const int, uint4*, const int64_t, const int64_t);
 
-// Vectors per thread per iteration, so that each thread keeps about 4 to 16
-// 16-byte loads in flight.  Measured on GB300 at 8 MiB per rank: W = 2 and 4
-// are faster with 4 and 2 vectors, W = 8 with 1 (12.2 against 12.4 us; fewer
-// registers give more resident CTAs), W = 16 with 1.
-constexpr int vectors_for(int W) { return W == 1 || W == 2 ? 4 : (W == 4 ? 2 : 1); }
+// Vectors per thread per iteration (U), so that each thread keeps 8 to 32
+// 16-byte loads in flight.  Measured on GB300 with equal shares and the
+// first-pass prefetch (graph replay over cold inputs, bf16, N = 8192): W = 2
+// is fastest with 4 (4.13 us at 8 MiB per rank; 5.58 with 1), W = 4 with 4
+// (14.0 against 14.3 us with 2 at 16 MiB), W = 16 with 2 (11.3 against
+// 13.2 us with 1 at 4 MiB; 4 and 8 were slower).  W = 8 keeps 1: with 2 it
+// ran 2 % faster alone in one buffer layout but made the reduce + fused step
+// slower in another (26.33 against 25.94 us).
+constexpr int vectors_for(int W) { return W <= 4 ? 4 : (W == 16 ? 2 : 1); }
 
 template <int DT>
 ReduceFn pick(int W) {
