@@ -54,7 +54,9 @@ def test_push_scrubs_and_packs_like_the_oracle(car):
 
 
 @pytest.mark.parametrize("W,M,N", [(2, 1, 2048), (8, 1, 8192), (4, 3, 1544), (16, 2, 1024), (5, 400, 512),
-                                   (8, 40, 8192), (3, 1, 8)])
+                                   (8, 40, 8192), (3, 1, 8),
+                                   # rows split over clusters of 8 and 4 for every row of a batch
+                                   (8, 16, 8192), (4, 16, 4096)])
 @pytest.mark.parametrize("missing", [False, True])
 def test_round_matches_the_oracle(car, W, M, N, missing):
     wl, xs, res, w = _inputs(W, M, N, 10 + W + M)

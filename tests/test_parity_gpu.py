@@ -159,6 +159,8 @@ FUSED_CASES = [
     # row with two vectors per thread (W=8), 1024 threads (W=4), a cluster of
     # two where no two-vector instance exists (W=16)
     (8, 64, 8192, "bf16"), (8, 180, 8192, "bf16"), (4, 150, 8192, "bf16"), (16, 40, 8192, "bf16"),
+    # automatic clusters of 8 and 4 CTAs for every row of a small batch
+    (8, 16, 8192, "bf16"), (2, 32, 8192, "bf16"), (8, 12, 4096, "fp16"),
 ]
 
 
