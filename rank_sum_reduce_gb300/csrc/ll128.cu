@@ -113,6 +113,19 @@ __global__ void __launch_bounds__(kWireThreads)
   const int flag_src = lane | 7;
   const int64_t pairs = (lines + 1) / 2;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  // While the previous grid of the stream finishes: the lines of this warp's
+  // first pair of line pairs, every rank, into L2 (one request per line, from
+  // its first lane).  Measured in graph replay over cold wires: W = 16 at
+  // 4 MiB per rank 13.3 -> 12.4 us, W = 8 at 8 MiB 13.6 -> 13.2 us, at
+  // 64 MiB 99.9 -> 99.1 us.
+  {
+    const int64_t p = 2 * (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) + (lane >> 4);
+    if (p < pairs && 2 * p + (c >> 3) < lines && (c & 7) == 0) {
+#pragma unroll
+      for (int r = 0; r < R; r++)
+        if (r < n) prefetch_line_l2(static_cast<const uint8_t*>(wires.p[r]) + p * 256 + 16 * c);
+    }
+  }
   pdl_wait_and_release();
   prepare_next_log(log, slot);
   for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
