@@ -27,9 +27,15 @@ namespace {
 __global__ void __launch_bounds__(kWireThreads)
     ll_encode_kernel(const uint4* __restrict__ data, const int64_t nvec, const uint32_t flag,
                      uint4* __restrict__ wire) {
-  pdl_wait_and_release();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  // While the previous grid of the stream finishes: this warp's first 32
+  // data vectors into L2, one request per 128 bytes (64 MiB: 34.8 -> 32.8 us).
+  {
+    const int64_t i = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32 + lane;
+    if (i < nvec && (lane & 7) == 0) prefetch_line_l2(data + i);
+  }
+  pdl_wait_and_release();
   for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 32 < nvec; w += nwarps) {
     const int64_t i = w * 32 + lane;
     const uint4 d = i < nvec ? ld_stream(data + i) : make_uint4(0u, 0u, 0u, 0u);
