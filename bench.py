@@ -23,6 +23,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -88,10 +89,15 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the dominant kernel's code (its sources with comments and
+    blank lines removed): the key under which profiles/dram_traffic.json
+    holds the ncu counters taken on that code."""
     h = hashlib.sha256()
     for f in ("fused.cu", "fused_tma.cu", "car_device.cuh"):
-        with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+        h.update("\n".join(line for line in lines if line).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,11 +11,12 @@
 // GB300 design, differing from the page: the page gives a whole row to one
 // program and leaves the rest of the GPU idle at M = 1.  Here a row can be
 // split over a thread-block cluster of up to 8 CTAs on different SMs; each CTA
-// reduces its slice, and the partial sums of squares meet through distributed
-// shared memory behind one cluster barrier per row.  With many rows, one CTA
-// takes a row and CTAs loop over rows (grid capped at the resident count).
-// h never leaves registers.  Roofline: HBM, (W + 1 + outputs) * 16 bytes per
-// vector plus the weight row.
+// reduces its slice and pushes its partial sum of squares into every peer's
+// shared memory (st.async, counted on the peer's mbarrier), so the row's total
+// is one one-way hop away.  With many rows, one CTA takes a row and CTAs loop
+// over rows (grid capped at the resident count).  Each CTA's first row is
+// requested into L2 before the PDL wait.  h never leaves registers.
+// Roofline: HBM, (W + 1 + outputs) * 16 bytes per vector plus the weight row.
 #include "car_device.cuh"
 #include "car_launch.h"
 

@@ -14,9 +14,12 @@
 //    reduce, normalise and store;
 //  * consumer warps own fixed 16-byte columns of the row: they fold each rank
 //    slice into fp32 accumulators in rank order as it lands, add the
-//    residual, store ar / residual_out, then meet at a named barrier for the
+//    residual, store ar / residual_out, then meet at two mbarriers for the
 //    row's sum of squares and store norm_out.  The weight row stays in
-//    registers for the whole kernel.
+//    registers for the whole kernel.  At W = 8 the last kRegSlices slices of
+//    a row skip the ring: the consumers load their own columns of them;
+//  * before the PDL wait, each CTA asks L2 for its first row, so that row's
+//    HBM latency passes while the previous grid of the stream finishes.
 //
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that runs out sets bit 0 of *err, stops the CTA's producer, waits (bounded
