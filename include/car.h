@@ -320,8 +320,13 @@ car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int 
 
 /* Wait for `stream` and report whether any kernel of this handle gave up one
  * of its bounded waits since the last car_sync (CAR_ERR_TIMEOUT; the flag is
- * then cleared).  The pipelined fused kernel bounds every wait on its
- * shared-memory barriers to about one second. */
+ * then cleared).  Each wait is bounded to about one second: the pipelined
+ * fused kernel's waits on its shared-memory barriers (it then stops and
+ * leaves its remaining rows unwritten), and the waits of the fused row kernel
+ * and the Lamport receive for the partials of a split row's other CTAs (the
+ * row's norm_out is then NaN, or the Lamport row is reported stale for every
+ * rank).  None of these waits runs out unless a CTA of the same launch has
+ * stopped making progress. */
 car_status car_sync(car_ctx* h, void* stream);
 
 #ifdef __cplusplus
