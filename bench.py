@@ -88,17 +88,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of the dominant kernel's code (its sources with comments and
-    blank lines removed): the key under which profiles/dram_traffic.json
-    holds the ncu counters taken on that code."""
+def code_digest(texts):
+    """Hash of C++ sources with comments and blank lines removed."""
     h = hashlib.sha256()
-    for f in ("fused.cu", "fused_tma.cu", "car_device.cuh"):
-        with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f)) as fh:
-            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+    for text in texts:
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
         h.update("\n".join(line for line in lines if line).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    """Digest of the dominant kernel's code: the key under which
+    profiles/dram_traffic.json holds the ncu counters taken on that code."""
+    texts = []
+    for f in ("fused.cu", "fused_tma.cu", "car_device.cuh"):
+        with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f)) as fh:
+            texts.append(fh.read())
+    return code_digest(texts)
 
 
 def ncu_traffic():
