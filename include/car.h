@@ -310,7 +310,8 @@ const char* car_last_error(void);
  * CTA whole rows, 2 splits every row over a CTA pair (needs an even number of
  * 16-byte columns); threads and vpt must be 0; needs N*s <= 100 KiB per CTA.
  * CAR_FUSED_AUTO (all fields 0) restores the automatic choice: the pipeline
- * with whole rows when M exceeds the SM count, else rows: a row split over a
+ * with whole rows when M exceeds the SM count and a row is larger than 8 KB
+ * (N*s > 8192), else rows: a row split over a
  * cluster of 8 or 4 CTAs while each CTA keeps at least 128 16-byte vectors,
  * the CTAs fit in 7/8 of the SMs, and M <= 16 or a row brings at least 48 KB
  * of inputs; one CTA per row otherwise.

@@ -181,13 +181,23 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
   return (int64_t)sh.threads * sh.vpt >= chunk;
 }
 
-// The pipelined kernel is faster once there are more rows than SMs.  Measured
-// on GB300 against the row kernel (both fetching their first row into L2
-// before the PDL wait), N = 8192 bf16: at M = 152, W = 8 5.8 (rows) against
-// 6.5 us (pipeline), W = 2 3.3 against 3.8; at M = 184, W = 8 8.2 against
-// 7.5, W = 2 5.3 against 4.5; at M = 456, W = 8 15.4 against 13.4.
+// The pipelined kernel is faster once there are more rows than SMs and a row
+// slice (N * s bytes, one bulk copy per rank) is larger than 8 KB.  Measured on
+// GB300 against the row kernel (both fetching their first row into L2 before
+// the PDL wait), N = 8192 bf16: at M = 152, W = 8 5.8 (rows) against 6.5 us
+// (pipeline), W = 2 3.3 against 3.8; at M = 184, W = 8 8.2 against 7.5, W = 2
+// 5.3 against 4.5; at M = 456, W = 8 15.4 against 13.4; at M = 1024 28.2
+// (pipeline) against 32.3; 12 KB slices, W = 8, M = 1024, N = 6144 bf16: 21.7
+// against 25.9; W = 4, M = 1024, N = 3072 fp32: 14.9 against 18.2.  With 8 KB
+// slices and smaller the persistent CTA finishes
+// its rows one after another (each behind the row statistic's barriers), and
+// the row kernel, many CTAs per SM, keeps more rows in flight: W = 4,
+// M = 1024, N = 4096 bf16 11.8 (rows) against 13.0 us; W = 8, M = 4096,
+// N = 2048 29.2 against 46.1; W = 2, M = 4096, N = 1024 8.9 against 27.4; a
+// deeper ring with several issuing lanes did not close the gap.
 int auto_fused_kernel(const car_ctx* h) {
-  return (h->tma_ok && h->M > (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
+  const bool big_slices = h->N * (int64_t)h->es > 8192;
+  return (h->tma_ok && big_slices && h->M > (int64_t)h->num_sms) ? CAR_FUSED_PIPELINE : CAR_FUSED_ROWS;
 }
 
 // Row-kernel shape for the Lamport receive step: the same rules as the fused
