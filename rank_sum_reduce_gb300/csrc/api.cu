@@ -189,9 +189,9 @@ bool shape_valid(int W, int V, const car::FusedShape& sh) {
 // 5.3 against 4.5; at M = 456, W = 8 15.4 against 13.4; at M = 1024 28.2
 // (pipeline) against 32.3; 12 KB slices, W = 8, M = 1024, N = 6144 bf16: 21.7
 // against 25.9; W = 4, M = 1024, N = 3072 fp32: 14.9 against 18.2.  With 8 KB
-// slices and smaller the persistent CTA finishes
-// its rows one after another (each behind the row statistic's barriers), and
-// the row kernel, many CTAs per SM, keeps more rows in flight: W = 4,
+// slices and smaller the persistent CTA finishes its rows one after another
+// (each behind the row statistic's barriers), and the row kernel, many CTAs
+// per SM, keeps more rows in flight: W = 4,
 // M = 1024, N = 4096 bf16 11.8 (rows) against 13.0 us; W = 8, M = 4096,
 // N = 2048 29.2 against 46.1; W = 2, M = 4096, N = 1024 8.9 against 27.4; a
 // deeper ring with several issuing lanes did not close the gap.
