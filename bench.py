@@ -99,10 +99,11 @@ def code_digest(texts):
 
 
 def kernel_source_hash():
-    """Digest of the dominant kernel's code: the key under which
-    profiles/dram_traffic.json holds the ncu counters taken on that code."""
+    """Digest of the dominant kernel's code (the pipelined fused kernel and the
+    headers it is built with): the key under which profiles/dram_traffic.json
+    holds the ncu counters taken on that code."""
     texts = []
-    for f in ("fused.cu", "fused_tma.cu", "car_device.cuh"):
+    for f in ("fused_tma.cu", "car_device.cuh", "car_launch.h"):
         with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f)) as fh:
             texts.append(fh.read())
     return code_digest(texts)

@@ -94,6 +94,19 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
 
   for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups, it++) {
     const int64_t rbase = row * (int64_t)p.vec_per_row;
+    // With more rows than CTAs: ask L2 for this CTA's piece of its next row
+    // (W ranks and the residual) while this one is reduced.  Many rows of 8 KB
+    // and less: W = 4, M = 1024, N = 4096 bf16 11.8 -> 10.1 us; M = 4096
+    // 38.4 -> 34.8 us; W = 2, M = 4096, N = 1024 8.9 -> 7.6 us.
+    {
+      const int64_t next = row + ngroups;
+      const int nvec = min(p.chunk, p.vec_per_row - col0);
+      if (next < p.rows && nvec > 0 && (int)threadIdx.x < n + 1) {
+        const int64_t off = next * (int64_t)p.vec_per_row + col0;
+        const int t = threadIdx.x;
+        prefetch_l2(t < n ? static_cast<const uint4*>(p.in.p[t]) + off : p.residual + off, (uint32_t)nvec * 16u);
+      }
+    }
 
     // 1. all loads of this thread's vectors: W ranks + residual
     uint4 raw[VPT][R];
