@@ -46,6 +46,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Ask L2 for this CTA's piece of `row` -- the n rank slices, the residual and,
+// when `weight`, the weight -- with one bulk prefetch per slice, issued by
+// threads 0 .. n (+1).  L2 is coherent for the whole GPU, so this may run
+// before the PDL wait.
+__device__ __forceinline__ void prefetch_row(const FusedParams& p, int n, int64_t row, int col0, bool weight) {
+  const int nvec = min(p.chunk, p.vec_per_row - col0);
+  const int t = threadIdx.x;
+  if (row >= p.rows || nvec <= 0 || t > n + (weight ? 1 : 0)) return;
+  const int64_t off = row * (int64_t)p.vec_per_row + col0;
+  const uint4* src = t < n ? static_cast<const uint4*>(p.in.p[t]) + off : (t == n ? p.residual + off : p.weight + col0);
+  prefetch_l2(src, (uint32_t)nvec * 16u);
+}
+
 template <int W, int VPT>
 constexpr int max_threads() {
   return (W > 0 && W <= 4 && VPT == 1) ? 1024 : 512;
@@ -78,35 +91,16 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
     __syncthreads();
     cluster_arrive();  // its wait, before the first partial is sent, covers the loads
   }
-  // While the previous grid of the stream finishes: this CTA's slice of its
-  // first row (W ranks, residual, weight) into L2, one bulk prefetch per slice.
-  {
-    const int64_t row0 = blockIdx.x / C;
-    const int nvec = min(p.chunk, p.vec_per_row - col0);
-    if (row0 < p.rows && nvec > 0 && (int)threadIdx.x < n + 2) {
-      const int64_t off = row0 * (int64_t)p.vec_per_row + col0;
-      const int t = threadIdx.x;
-      const uint4* src = t < n ? static_cast<const uint4*>(p.in.p[t]) + off : (t == n ? p.residual + off : p.weight + col0);
-      prefetch_l2(src, (uint32_t)nvec * 16u);
-    }
-  }
+  // While the previous grid of the stream finishes: this CTA's first row.
+  prefetch_row(p, n, blockIdx.x / C, col0, true);
   pdl_wait_and_release();
 
   for (int64_t row = blockIdx.x / C; row < p.rows; row += ngroups, it++) {
     const int64_t rbase = row * (int64_t)p.vec_per_row;
-    // With more rows than CTAs: ask L2 for this CTA's piece of its next row
-    // (W ranks and the residual) while this one is reduced.  Many rows of 8 KB
-    // and less: W = 4, M = 1024, N = 4096 bf16 11.8 -> 10.1 us; M = 4096
-    // 38.4 -> 34.8 us; W = 2, M = 4096, N = 1024 8.9 -> 7.6 us.
-    {
-      const int64_t next = row + ngroups;
-      const int nvec = min(p.chunk, p.vec_per_row - col0);
-      if (next < p.rows && nvec > 0 && (int)threadIdx.x < n + 1) {
-        const int64_t off = next * (int64_t)p.vec_per_row + col0;
-        const int t = threadIdx.x;
-        prefetch_l2(t < n ? static_cast<const uint4*>(p.in.p[t]) + off : p.residual + off, (uint32_t)nvec * 16u);
-      }
-    }
+    // With more rows than CTAs: this CTA's next row while this one is reduced.
+    // Many rows of 8 KB and less: W = 4, M = 1024, N = 4096 bf16 11.8 -> 10.1
+    // us; M = 4096 38.4 -> 34.8 us; W = 2, M = 4096, N = 1024 8.9 -> 7.6 us.
+    prefetch_row(p, n, row + ngroups, col0, false);
 
     // 1. all loads of this thread's vectors: W ranks + residual
     uint4 raw[VPT][R];
