@@ -64,8 +64,14 @@ constexpr int max_threads() {
   return (W > 0 && W <= 4 && VPT == 1) ? 1024 : 512;
 }
 
-template <int DT, int W, int VPT>
-__global__ void __launch_bounds__(max_threads<W, VPT>())
+// MINB: CTAs per SM the instance is compiled for.  W = 8 with one vector per
+// thread has a second instance held to two 512-thread CTAs per SM (64
+// registers, no spills) for one CTA per row over many rows, where a second
+// resident row pays: N = 4096 bf16, M = 256 5.40 -> 4.70 us, M = 1024 15.5 ->
+// 14.7 us.  Split rows keep the unbounded instance, whose latency is lower
+// (W = 8, M = 1, N = 8192: 1.92 against 2.02 us).
+template <int DT, int W, int VPT, int MINB>
+__global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
     reduce_residual_rmsnorm_kernel(const FusedParams p) {
   constexpr int E = Pack<DT>::kN;
   constexpr int R = W > 0 ? W : kMaxRanks;
@@ -199,32 +205,32 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
 using FusedFn = void (*)(const FusedParams);
 
 template <int DT>
-FusedFn pick_dt(int W, int vpt) {
+FusedFn pick_dt(int W, int vpt, int cluster) {
   if (vpt == 2) {
     switch (W) {
-      case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 2>;
-      case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 2>;
-      case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 2>;
-      case 8: return reduce_residual_rmsnorm_kernel<DT, 8, 2>;
+      case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 2, 1>;
+      case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 2, 1>;
+      case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 2, 1>;
+      case 8: return reduce_residual_rmsnorm_kernel<DT, 8, 2, 1>;
       default: return nullptr;
     }
   }
   if (vpt != 1) return nullptr;
   switch (W) {
-    case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 1>;
-    case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 1>;
-    case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 1>;
-    case 8: return reduce_residual_rmsnorm_kernel<DT, 8, 1>;
-    case 16: return reduce_residual_rmsnorm_kernel<DT, 16, 1>;
-    default: return reduce_residual_rmsnorm_kernel<DT, 0, 1>;
+    case 1: return reduce_residual_rmsnorm_kernel<DT, 1, 1, 1>;
+    case 2: return reduce_residual_rmsnorm_kernel<DT, 2, 1, 1>;
+    case 4: return reduce_residual_rmsnorm_kernel<DT, 4, 1, 1>;
+    case 8: return cluster == 1 ? reduce_residual_rmsnorm_kernel<DT, 8, 1, 2> : reduce_residual_rmsnorm_kernel<DT, 8, 1, 1>;
+    case 16: return reduce_residual_rmsnorm_kernel<DT, 16, 1, 1>;
+    default: return reduce_residual_rmsnorm_kernel<DT, 0, 1, 1>;
   }
 }
 
-FusedFn pick_fused(int dtype, int W, int vpt) {
+FusedFn pick_fused(int dtype, int W, int vpt, int cluster) {
   switch (dtype) {
-    case kBF16: return pick_dt<kBF16>(W, vpt);
-    case kFP16: return pick_dt<kFP16>(W, vpt);
-    default: return pick_dt<kFP32>(W, vpt);
+    case kBF16: return pick_dt<kBF16>(W, vpt, cluster);
+    case kFP16: return pick_dt<kFP16>(W, vpt, cluster);
+    default: return pick_dt<kFP32>(W, vpt, cluster);
   }
 }
 
@@ -258,7 +264,7 @@ bool fused_has_variant(int W, int vpt) {
 
 cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int num_sms, int* groups) {
   *groups = 0;
-  FusedFn fn = pick_fused(dtype, W, sh.vpt);
+  FusedFn fn = pick_fused(dtype, W, sh.vpt, sh.cluster);
   if (!fn) return cudaErrorInvalidValue;
   if (sh.cluster == 1) {
     int per_sm = 0;
@@ -283,7 +289,7 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
                          const void* weight, float eps, void* residual_out, void* norm_out,
                          void* ar_out, unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
                          const FusedShape& sh, cudaStream_t s) {
-  FusedFn fn = pick_fused(dtype, W, sh.vpt);
+  FusedFn fn = pick_fused(dtype, W, sh.vpt, sh.cluster);
   if (!fn) return cudaErrorInvalidValue;
   FusedParams p;
   p.in = in;
