@@ -161,6 +161,8 @@ FUSED_CASES = [
     (8, 64, 8192, "bf16"), (8, 180, 8192, "bf16"), (4, 150, 8192, "bf16"), (16, 40, 8192, "bf16"),
     # automatic clusters of 8 and 4 CTAs for every row of a small batch
     (8, 16, 8192, "bf16"), (2, 32, 8192, "bf16"), (8, 12, 4096, "fp16"),
+    # many 8 KB rows: the row kernel (W=8 at two CTAs per SM) loops over rows, prefetching the next
+    (8, 700, 4096, "bf16"), (4, 1000, 2048, "bf16"),
 ]
 
 
