@@ -846,7 +846,7 @@ def profile_case(name, launches=4):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1, help="GPUs (one process each under torchrun; replicas)")
-    ap.add_argument("--steps", type=int, default=20000, help="timed steps (reduce + fused on one batch each)")
+    ap.add_argument("--steps", type=int, default=20000, help="timed steps (one plain reduce and one fused call each)")
     ap.add_argument("--warmup", type=int, default=50, help="untimed steps before the timed region")
     ap.add_argument("--impl", choices=["car", "reference"], default="car",
                     help="car: the CUDA path; reference: the CPU oracle on the host cores")
