@@ -36,9 +36,11 @@ if ROOT not in sys.path:
 
 import workloads  # noqa: E402
 
-# steps per timed CUDA graph, and launches per per-kernel graph (see headline)
-GRAPH_STEPS = 64
+# most steps in one timed CUDA graph, and launches per per-kernel graph (see headline)
+MAX_GRAPH_STEPS = 1024
 GRAPH_LAUNCHES = 128
+# device time (ns) of the hold kernel queued ahead of a start event (see hold_device)
+HOLD_NS = 30000
 # steps of the end-to-end measurement run on this many streams in turn, so
 # one step's host copies overlap the next step's
 E2E_STREAMS = 3
@@ -229,6 +231,17 @@ def n_sets_for(set_bytes, minimum=3):
     return max(minimum, -(-2 * L2_BYTES // set_bytes) + 1)
 
 
+def hold_device():
+    """Queue a short device-side wait (torch's spin kernel) on the current
+    stream before a start event: the event and the work after it are then
+    submitted while the GPU is still busy, so the event marks the end of the
+    wait and host submission latency stays out of the timed region (the
+    blocking-kernel technique of GPU benchmark suites)."""
+    import torch
+
+    torch.cuda._sleep(int(HOLD_NS * 2.1))   # clock cycles at about 2.1 GHz
+
+
 def capture(torch, launches):
     """A CUDA graph of `launches` (callables taking a stream handle), captured
     on a side stream after one untimed run of the same launches."""
@@ -249,12 +262,14 @@ def headline(arm, wl, steps, warmup, rank, world):
     """Timed steps: plain reduce + fused reduce/residual/RMSNorm on rotating sets
     (the two calls of a step on different sets: see step_fns).
 
-    Steps run from CUDA graphs: one graph holds a step on each of the R input
-    sets in turn, single-step graphs cover a remainder, so the timed region
-    (one start and one end event) runs exactly `steps` steps.  Each kernel's
-    average launch duration comes from graphs of R launches of that kernel
-    alone, timed the same way.  Graphs keep host launch overhead out of the
-    device timeline."""
+    The timed region replays one CUDA graph that holds exactly `steps` steps
+    (for more than MAX_GRAPH_STEPS steps, a graph of a whole number of set
+    rotations replayed several times, then one graph of the rest), between one
+    start and one end event.  Warm-up runs its own graph of `warmup` steps,
+    and the timed steps continue the set rotation where it stopped.  Each
+    kernel's average launch duration comes from graphs of at least
+    GRAPH_LAUNCHES launches of that kernel alone, timed the same way.  Graphs
+    keep host launch overhead out of the device timeline."""
     torch, car, lib = arm.torch, arm.car, arm.lib
     set_bytes = (wl.W + 1) * wl.data_bytes + 3 * wl.data_bytes
     R = n_sets_for(set_bytes)
@@ -281,44 +296,43 @@ def headline(arm, wl, steps, warmup, rank, world):
                 raise RuntimeError(car.car_last_error())
         return run
 
-    # One graph per input set holding one step, and one graph holding the
-    # sequence of steps over the R sets several times over (at least
-    # GRAPH_STEPS steps): the timed region replays the long graph and then
-    # single-step graphs for the remainder, so it runs exactly `steps` steps.
-    # Each graph boundary leaves a gap on the device and breaks the PDL chain
-    # (the next graph's first kernel cannot overlap the last one's tail), so
-    # graphs of only R steps would charge that gap to every R steps.
-    rep_steps = max(1, -(-GRAPH_STEPS // R))
-    rep_launch = max(1, -(-GRAPH_LAUNCHES // R))
-    per_graph = R * rep_steps
     # Step i runs the reduce on set i and the fused op on set i + R/2, so no
     # input line of the fused call is still in L2 from the reduce call just
     # before it (both read the W ranks; with the same set in both calls the
     # step runs about 0.6 us faster at m512_w8 from that reuse).  Over R steps
     # every set gets both calls.
     def step_fns(i):
-        return [reduce_fn(sets[i]), fused_fn(sets[(i + R // 2) % R])]
+        return [reduce_fn(sets[i % R]), fused_fn(sets[(i + R // 2) % R])]
 
-    one_step = [capture(torch, step_fns(i)) for i in range(R)]
-    all_sets = capture(torch, [fn for _ in range(rep_steps) for i in range(R) for fn in step_fns(i)])
+    def steps_graph(first, count):
+        return capture(torch, [fn for i in range(first, first + count) for fn in step_fns(i)])
+
+    # A graph boundary leaves a gap on the device and breaks the PDL chain
+    # (the next graph's first kernel cannot overlap the last one's tail), so
+    # the timed steps sit in as few graphs as possible: one for up to
+    # MAX_GRAPH_STEPS steps.
+    chunk = steps if steps <= MAX_GRAPH_STEPS else (MAX_GRAPH_STEPS // R) * R
+    n_chunks, rest = divmod(steps, chunk)
+    warm = steps_graph(0, warmup)
+    body = steps_graph(warmup, chunk)
+    tail = steps_graph(warmup + n_chunks * chunk, rest) if rest else None
+    rep_launch = max(1, -(-GRAPH_LAUNCHES // R))
     reduce_all = capture(torch, [reduce_fn(S) for _ in range(rep_launch) for S in sets])
     fused_all = capture(torch, [fused_fn(S) for _ in range(rep_launch) for S in sets])
     cs = torch.cuda.current_stream()
 
-    def run_steps(n):
-        for _ in range(n // per_graph):
-            all_sets.replay()
-        for i in range(n % per_graph):
-            one_step[i % R].replay()
-
-    run_steps(warmup)
+    warm.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
+    hold_device()
     e0.record(cs)
-    run_steps(steps)
+    for _ in range(n_chunks):
+        body.replay()
+    if tail is not None:
+        tail.replay()
     e1.record(cs)
     torch.cuda.synchronize()
     barrier(world)
@@ -330,6 +344,8 @@ def headline(arm, wl, steps, warmup, rank, world):
         launches = R * rep_launch
         reps = max(1, steps // launches)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        hold_device()
         a.record(cs)
         for _ in range(reps):
             graph.replay()
@@ -342,10 +358,11 @@ def headline(arm, wl, steps, warmup, rank, world):
     status = car.car_sync(h, cs.cuda_stream)
     if status != car.CAR_OK:
         raise RuntimeError(f"car_sync: {car.car_status_string(status)}")
-    del one_step, all_sets, reduce_all, fused_all
+    del warm, body, tail, reduce_all, fused_all
     car.check(car.car_destroy(h), "car_destroy")
     return {"region_ms": region_ms, "reduce_ms": reduce_ms, "fused_ms": fused_ms, "sets": R, "set_bytes": set_bytes,
-            "t0": t0, "t1": t1, "launches": 2 * steps}
+            "t0": t0, "t1": t1, "launches": 2 * steps, "graphs": n_chunks + (1 if rest else 0),
+            "steps_per_graph": chunk}
 
 
 def e2e(arm, wl, steps, warmup, streams=1):
@@ -478,6 +495,48 @@ def latency_row(arm, wl, outputs, calls=12000):
             "GBps": round(set_bytes / (us * 1e-6) / 1e9, 1),
             "stream_launch_us_per_call": round(stream_us, 3), "host_us_per_call": round(host_us, 3),
             "l2": "cold (sets exceed 2x L2)" if n * set_bytes > 2 * L2_BYTES else "partly warm"}
+
+
+def isolated_latency(arm, wl, outputs, calls=200, n_sets=4):
+    """Device time of single, isolated fused calls: `calls` times, L2 is
+    flushed (a read of twice its size), a hold kernel is queued, then the
+    start event, one CUDA-graph replay holding one call (buffer sets
+    rotating), and the end event.  Returns the median and the 95th percentile
+    in us, and the samples' minimum and maximum."""
+    torch, car = arm.torch, arm.car
+    sets = make_sets(torch, wl, arm.dev, n_sets, outputs=("ar", "ro", "no"))
+    c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
+    lib, h = arm.lib, c.h
+    eps = ctypes.c_float(wl.eps)
+
+    def call_fn(S):
+        tbl = Arm.table([x.data_ptr() for x in S["xs"]])
+        args = (S["res"].data_ptr(), S["w"].data_ptr(), eps, S["ro"].data_ptr(), S["no"].data_ptr(),
+                S["ar"].data_ptr() if outputs == 3 else None)
+
+        def run(stream):
+            if lib.car_reduce_residual_rmsnorm(h, tbl, *args, stream):
+                raise RuntimeError(car.car_last_error())
+        return run
+
+    graphs = [capture(torch, [call_fn(S)]) for S in sets]
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=arm.dev)
+    cs = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(evs):
+        flush.sum()
+        hold_device()
+        a.record(cs)
+        graphs[i % n_sets].replay()
+        b.record(cs)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
+    c.sync()   # raises if a bounded wait ran out
+    del graphs, flush
+    c.close()
+    return {"median_us": round(statistics.median(us), 3), "p95_us": round(us[min(len(us) - 1, int(0.95 * len(us)))], 3),
+            "min_us": round(us[0], 3), "max_us": round(us[-1], 3), "calls": calls}
 
 
 def timed(torch, fn, iters):
@@ -687,21 +746,32 @@ def ll128_misaligned_row(arm, M, launches, reps=5):
     return row
 
 
-def ll_row(arm, iters=20):
-    """LL encode + validate/decode/reduce at the headline shape (W=8, 8 MB per rank);
-    encode time per call from graph replay of 64 calls over the 8 ranks."""
+def ll_row(arm, reps=5):
+    """LL encode + validate/decode/reduce at the headline shape (W=8, 8 MB per
+    rank), µs per call from graph replay.  Both rotate over sets of rank data
+    and wires whose total exceeds 2x L2, so every call reads from HBM: the
+    decode over 3 sets of 8 wires (128 MiB each), the encode over the 24
+    (data, wire) pairs of those sets."""
     torch, car = arm.torch, arm.car
     wl = workloads.WORKLOADS[HEADLINE]
     D = wl.data_bytes
-    xs = [workloads.make_x(wl, r, arm.dev) for r in range(wl.W)]
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
-    wires = [torch.empty(c.ll_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(wl.W)]
-    g = capture(torch, [(lambda x, wv: (lambda s: c.ll_encode(x, 7, wv, stream=s)))(xs[i % wl.W], wires[i % wl.W])
-                        for i in range(8 * wl.W)])
-    enc_ms = timed(torch, lambda i: g.replay(), 5) / (8 * wl.W)
-    del g
-    out = torch.empty_like(xs[0])
-    dec_ms = timed(torch, lambda i: c.ll_decode_reduce(wires, 7, out), iters)
+    n_sets = max(3, -(-2 * L2_BYTES // (wl.W * c.ll_wire_bytes)) + 1)
+    xs = [workloads.make_x(workloads.custom(wl.W, wl.M, wl.N, wl.dtype, seed=wl.seed + k), r, arm.dev)
+          for k in range(n_sets) for r in range(wl.W)]
+    wires = [torch.empty(c.ll_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in xs]
+    outs = [torch.empty_like(xs[0]) for _ in range(n_sets)]
+    pairs = len(xs)
+    enc = capture(torch, [(lambda x, wv: (lambda s: c.ll_encode(x, 7, wv, stream=s)))(xs[i % pairs], wires[i % pairs])
+                          for i in range(-(-64 // pairs) * pairs)])
+    n_enc = -(-64 // pairs) * pairs
+    enc_ms = timed(torch, lambda i: enc.replay(), reps) / n_enc
+    del enc
+    n_dec = -(-32 // n_sets) * n_sets
+    dec = capture(torch, [(lambda k: (lambda s: c.ll_decode_reduce(wires[k * wl.W:(k + 1) * wl.W], 7, outs[k],
+                                                                   stream=s)))(i % n_sets) for i in range(n_dec)])
+    dec_ms = timed(torch, lambda i: dec.replay(), reps) / n_dec
+    del dec
     n_stale, _ = c.ll_report()
     c.close()
     dec_bytes = wl.W * ll_wire_bytes(D) + D
@@ -709,7 +779,53 @@ def ll_row(arm, iters=20):
     return {"workload": "ll_" + wl.name, "decode_reduce_ms": round(dec_ms, 4),
             "decode_reduce_GBps": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
             "encode_ms_per_rank": round(enc_ms, 4), "encode_GBps": round(enc_bytes / (enc_ms * 1e-3) / 1e9, 1),
-            "stale_reported": n_stale, "l2": "8 MB per rank: wires 16 MB each, working set above L2"}
+            "stale_reported": n_stale,
+            "l2": f"cold: decode rotates over {n_sets} sets of {wl.W} wires ({n_sets * wl.W * ll_wire_bytes(D) >> 20} MiB), "
+                  f"encode over {pairs} (data, wire) pairs"}
+
+
+def noalloc_row(arm, reps=5):
+    """The allocation-free LL128 decode-reduce against the handle's, µs per
+    call from graph replay of 64 calls on the same wires: a small message
+    (W=4, 74 KB per rank, in L2) and the headline shape (W=8, 8 MiB per rank,
+    wires rotating over sets above 2x L2).  The allocation-free call adds a
+    memset before and a copy after its kernel."""
+    torch, car = arm.torch, arm.car
+    out = {}
+    for name, (W, M, N, n_sets) in {"small_w4_74KB": (4, 37, 1000, 1), "m512_w8": (8, 512, 8192, 3)}.items():
+        wl = workloads.custom(W, M, N, "bf16", seed=31)
+        c = car.Car(W, M, N, "bf16")
+        x = workloads.make_x(wl, 0, arm.dev)
+        wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=arm.dev) for _ in range(W * n_sets)]
+        for wv in wires:
+            c.ll128_encode(x, 7, wv)
+        o = torch.empty_like(x)
+        cap = 64
+        rep = torch.zeros(16 + 8 * cap, dtype=torch.uint8, device=arm.dev)
+
+        def handle_fn(k):
+            return lambda s: c.ll128_decode_reduce(wires[k * W:(k + 1) * W], 7, o, stream=s)
+
+        def noalloc_fn(k):
+            ptrs = [wv.data_ptr() for wv in wires[k * W:(k + 1) * W]]
+
+            def run(s):
+                st = car.car_ll128_decode_reduce_noalloc(W, M, N, car.CAR_BF16, ptrs, 7, 1, o.data_ptr(),
+                                                         rep.data_ptr(), cap, s)
+                if st:
+                    raise RuntimeError(car.car_last_error())
+            return run
+
+        row = {}
+        for kind, fn in (("handle_us", handle_fn), ("noalloc_us", noalloc_fn)):
+            fn(0)(torch.cuda.current_stream().cuda_stream)   # first call on the device: set-up outside capture
+            g = capture(torch, [fn(i % n_sets) for i in range(64)])
+            row[kind] = round(timed(torch, lambda i: g.replay(), reps) * 1000.0 / 64, 3)
+            del g
+        row["extra_us"] = round(row["noalloc_us"] - row["handle_us"], 3)
+        out[name] = row
+        c.close()
+    return out
 
 
 def barrier(world):
@@ -884,9 +1000,14 @@ def main():
     wl = workloads.WORKLOADS[HEADLINE]
 
     rows = {}
+    m1 = {}
     if not args.no_rows and rank == 0:
-        rows["m1_w2_fused_3out"] = latency_row(arm, workloads.WORKLOADS["m1_w2"], 3)
-        rows["m1_w8_fused"] = latency_row(arm, workloads.WORKLOADS["m1_w8"], 2)
+        for key, name, outputs in (("m1_w2_fused_3out", "m1_w2", 3), ("m1_w8_fused", "m1_w8", 2)):
+            wl_m1 = workloads.WORKLOADS[name]
+            rows[key] = latency_row(arm, wl_m1, outputs)
+            rows[key]["isolated"] = isolated_latency(arm, wl_m1, outputs)
+            m1[name] = {"median_us": rows[key]["isolated"]["median_us"], "p95_us": rows[key]["isolated"]["p95_us"],
+                        "b2b_us_per_call": rows[key]["us_per_call"]}
         rows["lamport_m1_w2"] = lamport_row(arm, workloads.WORKLOADS["m1_w2"])
         rows["lamport_m1_w8"] = lamport_row(arm, workloads.WORKLOADS["m1_w8"])
         rows["m2048_w4_fp32_fused"] = fused_fp32_row(arm)
@@ -896,6 +1017,7 @@ def main():
         rows["fused_w4_page_shapes"] = page_shapes_row(arm)
         rows["ll128_misaligned_1MiB"] = ll128_misaligned_row(arm, 64, 256)
         rows["ll128_misaligned_64MiB"] = ll128_misaligned_row(arm, 4096, 16)
+        rows["ll128_noalloc_vs_handle"] = noalloc_row(arm)
         torch.cuda.empty_cache()
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -944,7 +1066,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{wl.name}: W={wl.W} rank buffers, M={wl.M}, N={wl.N}, bf16; step = plain "
                                "reduce (ar) + fused reduce+residual+RMSNorm (residual_out, norm_out)",
-                   "timing": "steps replayed from CUDA graphs of >= 64 steps cycling over the input sets; events around all steps",
+                   "timing": f"the K steps replayed from {H['graphs']} CUDA graph(s) of {H['steps_per_graph']} steps "
+                             "cycling over the input sets, after a graph of the W warm-up steps; one start and one "
+                             "end event around them, a hold kernel queued before the start event",
                    "storage": wl.dtype, "accumulate": "f32", "eps": wl.eps,
                    "l2": f"inputs rotate over {H['sets']} sets of {H['set_bytes'] >> 20} MiB (> 2x L2); "
                          f"a step's fused call reads the set {H['sets'] // 2} steps ahead of its reduce call's",
@@ -967,6 +1091,9 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "rows": rows,
+        # last, so that a truncated copy of the line keeps it: M=1 latency of
+        # the fused call per isolated call (median, P95) and back to back
+        "m1_latency": m1 or None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -206,7 +206,15 @@ car_status car_ll128_report(car_ctx* h, car_stale_report* out);
  * 16-byte count) that every GPU which loads the library keeps until the
  * process exits.  The first call on a device looks up that array's device
  * address and the device's SM count, with the device current; make that
- * first call before any stream capture on the device.
+ * first call before any stream capture on the device.  The address is kept
+ * for the life of the process, so the device must not be reset
+ * (cudaDeviceReset) after that first call: a reset can place the array
+ * elsewhere, and the kept address would then point at other memory.
+ *
+ * Cost against the handle path: a memset before the kernel (the count) and a
+ * device-to-device copy after it (the report).  Neither is a kernel, so
+ * programmatic dependent launch cannot overlap this call with its
+ * neighbours in the stream.
  *
  * Every call on a device shares the array and it keeps the last call's
  * contents.  Each call clears the count on `stream` before its launch, so

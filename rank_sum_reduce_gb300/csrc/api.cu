@@ -50,7 +50,7 @@ struct car_ctx {
   int fused_kernel;
   unsigned int* d_err;  // bounded-wait failures reported by kernels (device)
   int64_t ll128_lines;
-  int ll128_encode_grid, ll128_decode_grid;
+  int ll128_encode_grid[2], ll128_decode_grid[2];  // [1]: the misaligned instances
   int64_t ll_lines;
   int ll_encode_grid, ll_decode_grid;
   bool lamport_ok;              // bf16 and a row the Lamport receive kernel takes
@@ -327,12 +327,15 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   if ((e = car::two_shot_occupancy(h->dtype, W, &per_sm)) != cudaSuccess) return fail(e, "two-shot occupancy");
   h->two_shot_grid = clamp_grid((h->nvec + per_cta - 1) / per_cta, per_sm, h->num_sms);
 
-  if ((e = car::ll128_occupancy(h->dtype, W, &per_sm, &per_sm2)) != cudaSuccess) return fail(e, "ll128 occupancy");
   const int64_t pairs = (h->ll128_lines + 1) / 2;
   const int64_t warps_needed = (pairs + 1) / 2;
   const int64_t blocks_needed = (warps_needed + car::kWireThreads / 32 - 1) / (car::kWireThreads / 32);
-  h->ll128_decode_grid = clamp_grid(blocks_needed, per_sm, h->num_sms);
-  h->ll128_encode_grid = clamp_grid(blocks_needed, per_sm2, h->num_sms);
+  for (int mis = 0; mis < 2; mis++) {
+    if ((e = car::ll128_occupancy(h->dtype, W, mis != 0, &per_sm, &per_sm2)) != cudaSuccess)
+      return fail(e, "ll128 occupancy");
+    h->ll128_decode_grid[mis] = clamp_grid(blocks_needed, per_sm, h->num_sms);
+    h->ll128_encode_grid[mis] = clamp_grid(blocks_needed, per_sm2, h->num_sms);
+  }
 
   if ((e = car::ll_occupancy(h->dtype, W, &per_sm, &per_sm2)) != cudaSuccess) return fail(e, "ll occupancy");
   h->ll_decode_grid = clamp_grid((h->ll_lines + car::kWireThreads - 1) / car::kWireThreads, per_sm, h->num_sms);
@@ -503,7 +506,8 @@ car_status car_ll128_encode(car_ctx* h, const void* data, uint64_t flag, void* w
   if (st != CAR_OK) return st;
   if ((st = check_dev_elem(data, h->es)) != CAR_OK) return st;
   if ((st = check_dev(wire)) != CAR_OK) return st;
-  cudaError_t e = car::launch_ll128_encode(data, h->D, h->ll128_lines, flag, wire, h->ll128_encode_grid,
+  const int mis = aligned16(data) ? 0 : 1;
+  cudaError_t e = car::launch_ll128_encode(data, h->D, h->ll128_lines, flag, wire, h->ll128_encode_grid[mis],
                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll128_encode launch");
 }
@@ -516,7 +520,7 @@ car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_
   if (st != CAR_OK) return st;
   cudaError_t e = car::launch_ll128_decode_reduce(h->dtype, h->W, tbl, h->D, h->ll128_lines, expected_flag,
                                                   max_polls, ar_out, h->log[0], next_log_slot(h, 0),
-                                                  h->ll128_decode_grid, s);
+                                                  h->ll128_decode_grid[aligned16(ar_out) ? 0 : 1], s);
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "ll128_decode_reduce launch");
 }
 

@@ -247,12 +247,13 @@ DecodeFn pick_decode(int dtype, int W, bool mis = false) {
 
 }  // namespace
 
-cudaError_t ll128_occupancy(int dtype, int W, int* decode_blocks_per_sm, int* encode_blocks_per_sm) {
+cudaError_t ll128_occupancy(int dtype, int W, bool mis, int* decode_blocks_per_sm, int* encode_blocks_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W)), kWireThreads, 0);
+      decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W, mis)), kWireThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      encode_blocks_per_sm, reinterpret_cast<const void*>(ll128_encode_kernel<false>), kWireThreads, 0);
+      encode_blocks_per_sm,
+      reinterpret_cast<const void*>(mis ? ll128_encode_kernel<true> : ll128_encode_kernel<false>), kWireThreads, 0);
 }
 
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,

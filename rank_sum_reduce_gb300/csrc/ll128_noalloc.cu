@@ -38,7 +38,8 @@ struct DeviceState {
   bool ready;
   StaleLog* log;          // device address of g_noalloc_scratch on this device
   int num_sms;
-  int per_sm[3][5];       // decode blocks per SM by dtype and W instance (0 = not asked yet)
+  int per_sm[3][5][2];    // decode blocks per SM by dtype, W instance and output alignment
+                          // (the aligned or the misaligned-output kernel; 0 = not asked yet)
 };
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -62,7 +63,9 @@ int w_instance(int W) {
 
 // Once per device, with that device current: look up where the array lives
 // on the device (the host-side name is only a stand-in for it) and read the
-// SM count.  The first call on each device runs this.
+// SM count.  The first call on each device runs this, and the address is
+// kept for the life of the process (a device reset after that first call is
+// not supported: it could move the array).
 car_status setup(int dev, DeviceState** out) {
   if (dev < 0 || dev >= kMaxDevices) {
     set_last_error("car_ll128_decode_reduce_noalloc: device index beyond 63");
@@ -127,10 +130,11 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
     std::lock_guard<std::mutex> lk(g_mu);
     car_status s = setup(dev, &st);
     if (s != CAR_OK) return s;
-    int& per_sm = st->per_sm[dtype][w_instance(W)];
+    const bool mis = (reinterpret_cast<uintptr_t>(ar_out) & 15u) != 0;  // the instance launched below
+    int& per_sm = st->per_sm[dtype][w_instance(W)][mis ? 1 : 0];
     if (per_sm == 0) {
       int enc = 0;
-      e = ll128_occupancy(dtype, W, &per_sm, &enc);
+      e = ll128_occupancy(dtype, W, mis, &per_sm, &enc);
       if (e != cudaSuccess) {
         per_sm = 0;
         return cuda_error(e, "ll128 occupancy");
