@@ -502,7 +502,9 @@ def isolated_latency(arm, wl, outputs, calls=200, n_sets=4):
     flushed (a read of twice its size), a hold kernel is queued, then the
     start event, one CUDA-graph replay holding one call (buffer sets
     rotating), and the end event.  Returns the median and the 95th percentile
-    in us, and the samples' minimum and maximum."""
+    in us, the samples' minimum and maximum, and the median of the same
+    sequence with nothing between the two events (what the event pair itself
+    costs on the device)."""
     torch, car = arm.torch, arm.car
     sets = make_sets(torch, wl, arm.dev, n_sets, outputs=("ar", "ro", "no"))
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
@@ -522,21 +524,30 @@ def isolated_latency(arm, wl, outputs, calls=200, n_sets=4):
     graphs = [capture(torch, [call_fn(S)]) for S in sets]
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=arm.dev)
     cs = torch.cuda.current_stream()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
-    torch.cuda.synchronize()
-    for i, (a, b) in enumerate(evs):
-        flush.sum()
-        hold_device()
-        a.record(cs)
-        graphs[i % n_sets].replay()
-        b.record(cs)
-    torch.cuda.synchronize()
-    us = sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
+
+    def sample(with_call):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            flush.sum()
+            hold_device()
+            a.record(cs)
+            if with_call:
+                graphs[i % n_sets].replay()
+            b.record(cs)
+        torch.cuda.synchronize()
+        return sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
+
+    us = sample(True)
+    empty = sample(False)   # the same sequence with nothing between the events
     c.sync()   # raises if a bounded wait ran out
     del graphs, flush
     c.close()
-    return {"median_us": round(statistics.median(us), 3), "p95_us": round(us[min(len(us) - 1, int(0.95 * len(us)))], 3),
-            "min_us": round(us[0], 3), "max_us": round(us[-1], 3), "calls": calls}
+    med = statistics.median(us)
+    return {"median_us": round(med, 3), "p95_us": round(us[min(len(us) - 1, int(0.95 * len(us)))], 3),
+            "min_us": round(us[0], 3), "max_us": round(us[-1], 3), "calls": calls,
+            "empty_event_pair_median_us": round(statistics.median(empty), 3),
+            "net_median_us": round(med - statistics.median(empty), 3)}
 
 
 def timed(torch, fn, iters):
@@ -1006,8 +1017,9 @@ def main():
             wl_m1 = workloads.WORKLOADS[name]
             rows[key] = latency_row(arm, wl_m1, outputs)
             rows[key]["isolated"] = isolated_latency(arm, wl_m1, outputs)
-            m1[name] = {"median_us": rows[key]["isolated"]["median_us"], "p95_us": rows[key]["isolated"]["p95_us"],
-                        "b2b_us_per_call": rows[key]["us_per_call"]}
+            iso = rows[key]["isolated"]
+            m1[name] = {"median_us": iso["median_us"], "p95_us": iso["p95_us"],
+                        "empty_events_us": iso["empty_event_pair_median_us"], "b2b_us_per_call": rows[key]["us_per_call"]}
         rows["lamport_m1_w2"] = lamport_row(arm, workloads.WORKLOADS["m1_w2"])
         rows["lamport_m1_w8"] = lamport_row(arm, workloads.WORKLOADS["m1_w8"])
         rows["m2048_w4_fp32_fused"] = fused_fp32_row(arm)

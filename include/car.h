@@ -322,7 +322,8 @@ const char* car_last_error(void);
  * (N*s > 8192), else rows: a row split over a
  * cluster of 8 or 4 CTAs while each CTA keeps at least 128 16-byte vectors,
  * the CTAs fit in 7/8 of the SMs, and M <= 16 or a row brings at least 48 KB
- * of inputs; one CTA per row otherwise.
+ * of inputs; one CTA per row otherwise (with two vectors per thread where
+ * one vector per thread would need 1024 threads).
  * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_SIZE when the shape
  * does not cover a row or the row does not fit the ring. */
 car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int vpt);
@@ -337,6 +338,24 @@ car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int 
  * rank).  None of these waits runs out unless a CTA of the same launch has
  * stopped making progress. */
 car_status car_sync(car_ctx* h, void* stream);
+
+/* Test hook for the bounded wait of the fused row kernel (CAR_FUSED_ROWS
+ * with rows split over a cluster).  The pages have no such call: it serves
+ * the tests of the failure path that P2 "LL 如何发布和等待 flag" gives every
+ * spin (a wait that checks for abort instead of spinning forever).
+ *
+ * With cta in 0..7: the split row's partial exchange waits at most
+ * wait_limit_ns (1000 .. 1e9) instead of about one second, and CTA `cta` of
+ * the cluster that takes row `row` (0 .. M-1) pushes its partial delay_ns
+ * (at most CAR_TEST_MAX_DELAY_NS) late.  A peer whose wait runs out first
+ * sets the handle's error flag (car_sync then returns CAR_ERR_TIMEOUT),
+ * writes NaN for its columns of that row's norm_out, and then waits (bounded
+ * by about one second) until the late partial has landed before it goes on,
+ * so no partial reaches a CTA that has exited.  Every other output is
+ * unaffected.  With cta = -1 (and the other arguments 0) the default returns.
+ * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_HANDLE. */
+#define CAR_TEST_MAX_DELAY_NS 100000000ull /* 100 ms */
+car_status car_test_delay_partial(car_ctx* h, uint64_t wait_limit_ns, int cta, int64_t row, uint64_t delay_ns);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,7 @@ _SIGS = {
     "car_last_error": (ctypes.c_char_p, []),
     "car_tune_fused": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "car_sync": (ctypes.c_int, [_vp, _vp]),
+    "car_test_delay_partial": (ctypes.c_int, [_vp, ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64]),
     "car_lamport_buffer_bytes": (ctypes.c_size_t, [_vp]),
     "car_lamport_init": (ctypes.c_int, [_vp, _vp, _vp]),
     "car_lamport_push": (ctypes.c_int, [_vp, _vp, ctypes.c_int, ctypes.c_uint64, _vp, _vp]),
@@ -206,6 +207,10 @@ def car_tune_fused(h, kernel: int, cluster: int, threads: int, vpt: int) -> int:
 
 def car_sync(h, stream: int = 0) -> int:
     return _lib.car_sync(h, stream)
+
+
+def car_test_delay_partial(h, wait_limit_ns: int, cta: int, row: int, delay_ns: int) -> int:
+    return _lib.car_test_delay_partial(h, wait_limit_ns, cta, row, delay_ns)
 
 
 # ---------------------------------------------------------------------------

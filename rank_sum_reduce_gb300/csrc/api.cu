@@ -49,6 +49,7 @@ struct car_ctx {
   int fused_kernel_auto;  // CAR_FUSED_ROWS or CAR_FUSED_PIPELINE
   int fused_kernel;
   unsigned int* d_err;  // bounded-wait failures reported by kernels (device)
+  car::WaitHook hook;   // the fused row kernel's partial-exchange wait limit and test delay
   int64_t ll128_lines;
   int ll128_encode_grid[2], ll128_decode_grid[2];  // [1]: the misaligned instances
   int64_t ll_lines;
@@ -143,14 +144,24 @@ int round_up32(int64_t v) { return (int)((v + 31) / 32 * 32); }
 // N = 8192, M = 32 (c = 4) 2.26 / 2.45.  Where the rule keeps one CTA per row
 // it was as fast or faster: W = 4, N = 4096, M = 32: 2.09 against 2.20 with
 // four CTAs; W = 2, N = 2048, M = 1: 1.48 against 1.64 with two.
+//
+// With prefer_half_ctas, a shape that would need a 1024-thread CTA with one
+// vector per thread takes 512 threads with two vectors instead when that
+// instance exists.  Measured for the fused row kernel (one CTA per row, bf16,
+// N = 8192, graph replay over cold inputs, us per call, 512 x 2 against
+// 1024 x 1): W = 4, M = 128 3.51 / 3.61; W = 4, M = 64 2.74 / 2.85; W = 2,
+// M = 128 2.89 / 3.05.
 template <class HasVariant, class MaxThreads>
 car::FusedShape row_split_shape(int W, int64_t M, int V, int num_sms, HasVariant has_variant,
-                                MaxThreads max_threads) {
+                                MaxThreads max_threads, bool prefer_half_ctas) {
   auto fit = [&](int c, car::FusedShape* out) {
     const int chunk = (V + c - 1) / c;
     for (int vpt = 1; vpt <= 2; vpt++) {
       if (!has_variant(W, vpt)) continue;
       const int t = std::max(32, round_up32((chunk + vpt - 1) / vpt));
+      if (vpt == 1 && prefer_half_ctas && t > 512 && has_variant(W, 2) &&
+          std::max(32, round_up32((chunk + 1) / 2)) <= max_threads(W, 2))
+        continue;
       if (t <= max_threads(W, vpt)) {
         *out = car::FusedShape{c, t, vpt, 1};
         return true;
@@ -170,7 +181,7 @@ car::FusedShape row_split_shape(int W, int64_t M, int V, int num_sms, HasVariant
 }
 
 car::FusedShape auto_fused_shape(int W, int64_t M, int V, int num_sms) {
-  return row_split_shape(W, M, V, num_sms, car::fused_has_variant, car::fused_max_threads);
+  return row_split_shape(W, M, V, num_sms, car::fused_has_variant, car::fused_max_threads, true);
 }
 
 bool shape_valid(int W, int V, const car::FusedShape& sh) {
@@ -203,7 +214,7 @@ int auto_fused_kernel(const car_ctx* h) {
 // Row-kernel shape for the Lamport receive step: the same rules as the fused
 // row kernel, within the Lamport kernel's compiled instances.
 car::FusedShape auto_lamport_shape(int W, int64_t M, int V, int num_sms) {
-  return row_split_shape(W, M, V, num_sms, car::lamport_has_variant, car::lamport_max_threads);
+  return row_split_shape(W, M, V, num_sms, car::lamport_has_variant, car::lamport_max_threads, false);
 }
 
 car_status finish_fused_shape(car_ctx* h, car::FusedShape sh) {
@@ -307,6 +318,7 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   h->vec_per_row = (int)(N * es / 16);
   h->ll128_lines = (D + 119) / 120;
   h->ll_lines = D / 8;
+  h->hook = car::WaitHook{car::kWaitLimitNs, 0, 0, -1};
 
   auto fail = [&](cudaError_t e, const char* where) {
     for (auto*& p : h->log)
@@ -438,6 +450,21 @@ car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int 
   return st;
 }
 
+car_status car_test_delay_partial(car_ctx* h, uint64_t wait_limit_ns, int cta, int64_t row, uint64_t delay_ns) {
+  car_status st = check_handle(h);
+  if (st != CAR_OK) return st;
+  if (cta < 0) {
+    if (wait_limit_ns || row || delay_ns) return CAR_ERR_ARG;
+    h->hook = car::WaitHook{car::kWaitLimitNs, 0, 0, -1};
+    return CAR_OK;
+  }
+  if (cta > 7 || row < 0 || row >= h->M || wait_limit_ns < 1000 || wait_limit_ns > car::kWaitLimitNs ||
+      delay_ns > CAR_TEST_MAX_DELAY_NS)
+    return CAR_ERR_ARG;
+  h->hook = car::WaitHook{wait_limit_ns, delay_ns, row, cta};
+  return CAR_OK;
+}
+
 car_status car_sync(car_ctx* h, void* stream) {
   if (!live(h)) return CAR_ERR_HANDLE;
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
@@ -494,7 +521,7 @@ car_status car_reduce_residual_rmsnorm(car_ctx* h, const void* const* inputs, co
                               h->d_err, h->M, h->N, h->vec_per_row, h->tma, static_cast<cudaStream_t>(stream));
   else
     e = car::launch_fused(h->dtype, h->W, tbl, residual, weight, eps, residual_out, norm_out, ar_out, h->d_err,
-                          h->M, h->N, h->vec_per_row, h->fused, static_cast<cudaStream_t>(stream));
+                          h->M, h->N, h->vec_per_row, h->fused, h->hook, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CAR_OK : cuda_fail(e, "reduce_residual_rmsnorm launch");
 }
 

@@ -242,15 +242,26 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 // Wait, with cluster-scope acquire, for the phase of `bar` with the given
-// parity; false when it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool wait_cluster_phase(uint64_t* bar, uint32_t parity) {
+// parity; false when it has not completed within limit_ns.
+__device__ __forceinline__ bool wait_cluster_phase(uint64_t* bar, uint32_t parity,
+                                                   unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1; i < (1u << 30); i++) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((i & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Spin for about `ns` nanoseconds of %globaltimer (bounded by an iteration
+// count as well).
+__device__ __forceinline__ void spin_ns(unsigned long long ns) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 0; i < (1u << 30); i++) {
+    if (globaltimer() - t0 >= ns) return;
+    __nanosleep(256);
+  }
 }
 
 // ---------------------------------------------------------------------------

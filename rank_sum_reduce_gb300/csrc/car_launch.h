@@ -36,10 +36,18 @@ int fused_max_threads(int W, int vpt);
 bool fused_has_variant(int W, int vpt);
 // How many row groups of this shape can be resident at once (0 on error).
 cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int num_sms, int* groups);
+// The split-row partial exchange's wait limit, and the test hook that makes
+// one CTA push its partial late (delay_cta < 0: none).
+struct WaitHook {
+  unsigned long long wait_ns;
+  unsigned long long delay_ns;
+  int64_t delay_row;
+  int delay_cta;
+};
 cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
                          const void* weight, float eps, void* residual_out, void* norm_out,
                          void* ar_out, unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
-                         const FusedShape& sh, cudaStream_t s);
+                         const FusedShape& sh, const WaitHook& hook, cudaStream_t s);
 
 // ---- fused, many rows: TMA bulk copies into a shared-memory ring (fused_tma.cu) ----
 struct FusedTmaShape {

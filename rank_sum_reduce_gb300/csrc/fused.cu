@@ -38,6 +38,14 @@ struct FusedParams {
   int chunk;      // 16-byte vectors of a row handled by one CTA
   int cluster;    // CTAs per row
   int nranks;
+  // The bounded wait for a split row's partials, and a test hook that holds
+  // back one CTA's partial (see car_test_delay_partial): CTA `delay_cta` of
+  // the cluster that takes row `delay_row` pushes its partial `delay_ns`
+  // late.  delay_cta < 0: no delay.
+  unsigned long long wait_ns;
+  unsigned long long delay_ns;
+  int64_t delay_row;
+  int delay_cta;
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -164,16 +172,22 @@ __global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
       t = warp_sum(t);
       if (lane == 0) {
         if (C > 1) {
-          const uint32_t b = it & 1u;
+          const uint32_t b = it & 1u, par = (it >> 1) & 1u;
           mbar_arrive_expect_tx(&s_xbar[b], 4u * (uint32_t)C);
+          if (crank == p.delay_cta && row == p.delay_row) spin_ns(p.delay_ns);
           for (int r = 0; r < C; r++)
             st_async_f32(map_rank(&s_part[b][crank], (uint32_t)r), t, map_rank(&s_xbar[b], (uint32_t)r));
-          if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
+          if (wait_cluster_phase(&s_xbar[b], par, p.wait_ns)) {
             t = s_part[b][0];
             for (int r = 1; r < C; r++) t += s_part[b][r];
           } else {
             atomicOr(p.err, 1u);
             t = __int_as_float(0x7fc00000);  // NaN: this row's norm_out is not usable
+            // The missing partials may still come: wait (bounded again) until
+            // they have landed, so that none reaches this CTA's shared memory
+            // after it has exited and the barrier's phases stay in step for
+            // the next row.
+            if (!wait_cluster_phase(&s_xbar[b], par)) atomicOr(p.err, 2u);
           }
         }
         s_total = t;
@@ -288,7 +302,7 @@ cudaError_t fused_resident_groups(int dtype, int W, const FusedShape& sh, int nu
 cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* residual,
                          const void* weight, float eps, void* residual_out, void* norm_out,
                          void* ar_out, unsigned int* err, int64_t rows, int64_t cols, int vec_per_row,
-                         const FusedShape& sh, cudaStream_t s) {
+                         const FusedShape& sh, const WaitHook& hook, cudaStream_t s) {
   FusedFn fn = pick_fused(dtype, W, sh.vpt, sh.cluster);
   if (!fn) return cudaErrorInvalidValue;
   FusedParams p;
@@ -306,6 +320,10 @@ cudaError_t launch_fused(int dtype, int W, const RankPtrs& in, const void* resid
   p.chunk = (vec_per_row + sh.cluster - 1) / sh.cluster;
   p.cluster = sh.cluster;
   p.nranks = W;
+  p.wait_ns = hook.wait_ns;
+  p.delay_ns = hook.delay_ns;
+  p.delay_row = hook.delay_row;
+  p.delay_cta = hook.delay_cta;
   return launch_pdl(fn, (unsigned)(sh.groups * sh.cluster), (unsigned)sh.threads, 0, s, (unsigned)sh.cluster, p);
 }
 
