@@ -101,11 +101,12 @@ def code_digest(texts):
 
 
 def kernel_source_hash():
-    """Digest of the dominant kernel's code (the pipelined fused kernel and the
-    headers it is built with): the key under which profiles/dram_traffic.json
-    holds the ncu counters taken on that code."""
+    """Digest of the dominant kernel's code: fused_tma.cu (the pipelined fused
+    kernel, its launch shape and launcher) and car_device.cuh (the device
+    helpers it is built with).  The key under which
+    profiles/dram_traffic.json holds the ncu counters taken on that code."""
     texts = []
-    for f in ("fused_tma.cu", "car_device.cuh", "car_launch.h"):
+    for f in ("fused_tma.cu", "car_device.cuh"):
         with open(os.path.join(ROOT, "rank_sum_reduce_gb300", "csrc", f)) as fh:
             texts.append(fh.read())
     return code_digest(texts)
@@ -936,19 +937,37 @@ PROFILE_CASES = {
     "ll128_decode": (16, 1024, 8192, "bf16"),
     "ll_decode": (8, 512, 8192, "bf16"),
     "fused_fp32": (4, 2048, 4096, "fp32"),
+    # the headline kernels on the headline workload, rotating over 4 input sets (384 MiB)
+    "fused_m512_w8": (8, 512, 8192, "bf16"),
+    "reduce_m512_w8": (8, 512, 8192, "bf16"),
 }
 
 
 def profile_case(name, launches=4):
     """Run one workload's kernel `launches` times and exit: a small, fixed
-    command for ncu captures of kernels outside the headline step."""
+    command for ncu captures (the headline kernels one at a time, each launch
+    on the next of 4 input sets, and kernels outside the headline step)."""
     import torch
 
     import rank_sum_reduce_gb300 as car
 
     W, M, N, dt = PROFILE_CASES[name]
-    wl = workloads.custom(W, M, N, dt, seed=90)
     dev = torch.device("cuda", 0)
+    if name in ("fused_m512_w8", "reduce_m512_w8"):
+        wl = workloads.WORKLOADS[HEADLINE]
+        sets = make_sets(torch, wl, dev, 4)
+        with car.Car(wl.W, wl.M, wl.N, wl.dtype) as c:
+            for i in range(launches):
+                S = sets[i % 4]
+                if name == "fused_m512_w8":
+                    c.reduce_residual_rmsnorm(S["xs"], S["res"], S["w"], wl.eps, S["ro"], S["no"])
+                else:
+                    c.reduce(S["xs"], S["ar"])
+            torch.cuda.synchronize()
+            c.sync()
+        print(f"profile case {name}: {wl.name}, {launches} launches over 4 input sets")
+        return
+    wl = workloads.custom(W, M, N, dt, seed=90)
     xs = [workloads.make_x(wl, r, dev) for r in range(W)]
     out = torch.empty_like(xs[0])
     with car.Car(W, M, N, dt) as c:
@@ -981,9 +1000,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                     help="run one workload's kernel a few times and exit (for ncu captures)")
+    ap.add_argument("--profile-launches", type=int, default=4, help="launches of the --profile-case kernel")
     args = ap.parse_args()
     if args.profile_case:
-        profile_case(args.profile_case)
+        profile_case(args.profile_case, args.profile_launches)
         return
     if args.warmup < 3:
         args.warmup = 3

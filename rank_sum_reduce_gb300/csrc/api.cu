@@ -343,7 +343,7 @@ car_status car_create(int W, int64_t M, int64_t N, car_dtype dtype, car_ctx** ou
   const int64_t warps_needed = (pairs + 1) / 2;
   const int64_t blocks_needed = (warps_needed + car::kWireThreads / 32 - 1) / (car::kWireThreads / 32);
   for (int mis = 0; mis < 2; mis++) {
-    if ((e = car::ll128_occupancy(h->dtype, W, mis != 0, &per_sm, &per_sm2)) != cudaSuccess)
+    if ((e = car::ll128_occupancy(h->dtype, W, mis != 0, h->ll128_lines, &per_sm, &per_sm2)) != cudaSuccess)
       return fail(e, "ll128 occupancy");
     h->ll128_decode_grid[mis] = clamp_grid(blocks_needed, per_sm, h->num_sms);
     h->ll128_encode_grid[mis] = clamp_grid(blocks_needed, per_sm2, h->num_sms);

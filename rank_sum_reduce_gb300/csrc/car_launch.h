@@ -72,8 +72,9 @@ cudaError_t launch_fused_tma(int dtype, int W, const RankPtrs& in, const void* r
 constexpr int kWireThreads = 256;
 // Resident CTAs per SM of the decode and encode instances that a call with
 // 16-byte aligned (mis = false) or misaligned (mis = true) output / rank data
-// launches.
-cudaError_t ll128_occupancy(int dtype, int W, bool mis, int* decode_blocks_per_sm, int* encode_blocks_per_sm);
+// launches on a message of `lines` LL128 lines.
+cudaError_t ll128_occupancy(int dtype, int W, bool mis, int64_t lines, int* decode_blocks_per_sm,
+                            int* encode_blocks_per_sm);
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
                                 void* wire, int grid, cudaStream_t s);
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,

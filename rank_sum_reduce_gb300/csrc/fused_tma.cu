@@ -19,7 +19,8 @@
 //    registers for the whole kernel.  At W = 8 the last kRegSlices slices of
 //    a row skip the ring: the consumers load their own columns of them;
 //  * before the PDL wait, each CTA asks L2 for its first row, so that row's
-//    HBM latency passes while the previous grid of the stream finishes.
+//    HBM latency passes while the previous grid of the stream finishes (only
+//    when there is such a grid still running).
 //
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that runs out sets bit 0 of *err, stops the CTA's producer, waits (bounded
@@ -32,6 +33,11 @@ namespace {
 
 // Slices per row loaded by the consumers instead of bulk copies (see run_consumers).
 constexpr int kRegSlices = 3;
+// First-row L2 prefetch in the prologue: slices requested at once, and how
+// long the producer warp looks for the dependency wait's return before it
+// requests the rest (see the kernel's prologue).
+constexpr int kEarlyPrefetch = 2;
+constexpr unsigned long long kPrefetchGraceNs = 100;
 
 struct TmaParams {
   RankPtrs in;
@@ -336,6 +342,7 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
   float* s_part = s_warp + 16;                           // [2][2] partials of the cluster's CTAs
   float* s_total = s_part + 4;
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_total + 1);
+  volatile int* s_dep = s_abort + 1;   // set once the dependency wait has returned
 
   const int n = W > 0 ? W : p.nranks;
   const int nconsumer_warps = p.consumers >> 5;
@@ -352,21 +359,44 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
     mbar_init(&xbar[0], 1);  // completed by the local expect_tx arrive plus C x 4 bytes
     mbar_init(&xbar[1], 1);
     *s_abort = 0;
+    *s_dep = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (C > 1) cluster_barrier();  // peers' barriers exist before anyone arrives on them
   // While the previous grid of the stream finishes: this CTA's piece of its
-  // first row (W ranks, residual, weight) into L2, one bulk prefetch each.
-  if (group < p.rows && (int)threadIdx.x < n + 2) {
-    const int t = threadIdx.x;
+  // first row (W ranks, residual, weight) into L2, one bulk prefetch each, by
+  // the producer warp.  The first kEarlyPrefetch slices are requested at
+  // once; the rest only if the dependency wait has not returned within
+  // kPrefetchGraceNs, i.e. only when a previous grid is still running and
+  // the prefetch can use the HBM time its tail leaves idle.  With no grid
+  // before this one, prefetching the whole row only duplicates the first
+  // copies and delays them.  Measured on GB300 at W = 8, M = 512, N = 8192
+  // bf16 (cold launch: median of 24 ncu launches with caches flushed; step:
+  // plain reduce then this kernel, graph replay): whole row always 18.03 us
+  // cold, 25.97 us per step; none 17.07 us in graph replay of this kernel
+  // alone (against 14.65 with the prefetch); the whole row after a 100 ns
+  // grace 17.34 cold, 25.68 per step; two slices at once and the rest after
+  // the grace 17.18 cold, 25.54 per step (same box).  griddepcontrol.wait
+  // holds the whole warp that executes it, so thread 0 (consumer warp 0)
+  // waits and sets s_dep, and no lane of the producer warp waits before the
+  // warp has decided.
+  if (warp == nconsumer_warps && group < p.rows) {
+    const int q = lane < n ? lane : 0;
     const int64_t off = group * (int64_t)p.row_bytes + (int64_t)crank * slice;
-    const void* src = t < n    ? static_cast<const void*>(static_cast<const uint8_t*>(p.in.p[t]) + off)
-                      : t == n ? static_cast<const void*>(p.residual + off)
-                               : static_cast<const void*>(p.weight + (int64_t)crank * cols);
-    prefetch_l2(src, (uint32_t)slice);
+    const void* src = lane < n    ? static_cast<const void*>(static_cast<const uint8_t*>(p.in.p[q]) + off)
+                      : lane == n ? static_cast<const void*>(p.residual + off)
+                                  : static_cast<const void*>(p.weight + (int64_t)crank * cols);
+    if (lane < kEarlyPrefetch && lane < n + 2) prefetch_l2(src, (uint32_t)slice);
+    const unsigned long long t0 = globaltimer();
+    while (!*s_dep && globaltimer() - t0 < kPrefetchGraceNs) {
+    }
+    const bool still_waiting = __any_sync(0xFFFFFFFFu, !*s_dep);
+    if (still_waiting && lane >= kEarlyPrefetch && lane < n + 2) prefetch_l2(src, (uint32_t)slice);
   }
+  __syncwarp();
   pdl_wait_and_release();        // inputs may come from the previous kernel of the stream
+  if (threadIdx.x == 0) *s_dep = 1;
 
   if (warp == nconsumer_warps) {
     if (lane == 0) run_producer(p, ring, full, empty, s_abort, S, slice, n, crank, group, ngroups);

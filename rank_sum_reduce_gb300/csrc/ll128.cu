@@ -43,6 +43,15 @@ __device__ __forceinline__ uint4 shfl_down16(uint4 v, int by, int width) {
   return make_uint4(__shfl_down_sync(0xFFFFFFFFu, v.x, by, width), __shfl_down_sync(0xFFFFFFFFu, v.y, by, width),
                     __shfl_down_sync(0xFFFFFFFFu, v.z, by, width), __shfl_down_sync(0xFFFFFFFFu, v.w, by, width));
 }
+// Evict-first 16-byte store (st.global.cs): the line is not expected to be
+// read again soon from L2.
+__device__ __forceinline__ void st16_evict_first(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// Aligned rank data whose wire is at least this large per rank is encoded
+// by the streaming instance (see ll128_encode_kernel).
+constexpr int64_t kStreamWireBytes = 32ll << 20;
 __device__ __forceinline__ uint4 shfl_idx16(uint4 v, int src) {
   return make_uint4(__shfl_sync(0xFFFFFFFFu, v.x, src), __shfl_sync(0xFFFFFFFFu, v.y, src),
                     __shfl_sync(0xFFFFFFFFu, v.z, src), __shfl_sync(0xFFFFFFFFu, v.w, src));
@@ -61,7 +70,7 @@ __device__ __forceinline__ uint4 shfl_idx16(uint4 v, int src) {
 // that holds a data byte lies in the same page as that byte, so the load is
 // safe -- and rebuilds data vector c from blocks c and c + 1 (one lane
 // shuffle and a funnel shift), staying in registers.
-template <bool kMis>
+template <bool kMis, bool kStream>
 __global__ void __launch_bounds__(kWireThreads)
     ll128_encode_kernel(const uint8_t* __restrict__ data, const int64_t data_bytes,
                         const int64_t lines, const uint64_t flag, uint8_t* __restrict__ wire) {
@@ -77,26 +86,51 @@ __global__ void __launch_bounds__(kWireThreads)
     if (p < pairs && (c & 7) == 0 && doff < data_bytes) prefetch_line_l2(data + doff);
   }
   pdl_wait_and_release();
-  for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
-       wp += nwarps) {
-    const int64_t p = 2 * wp + (lane >> 4);
-    uint4 d = make_uint4(0u, 0u, 0u, 0u);
-    const int64_t doff = p * 240 + 16 * c;
-    if (!kMis) {
-      if (p < pairs && c < 15 && doff < data_bytes) d = ld_stream(data + doff);
-    } else {
-      const int m = (int)(reinterpret_cast<uintptr_t>(data) & 15u);
-      uint4 blk = make_uint4(0u, 0u, 0u, 0u);
-      if (p < pairs && doff - m < data_bytes) blk = ld_stream(data - m + doff);
-      const uint4 nxt = shfl_down16(blk, 1, 16);
-      if (p < pairs && c < 15 && doff < data_bytes) d = bytes_at(blk, nxt, m);
+  // The streaming instance (kStream: aligned data, a wire of at least
+  // kStreamWireBytes per rank, so that a few ranks' wires overflow L2 anyway)
+  // keeps the loads of two warp iterations (warp pairs wp and wp + nwarps) in
+  // flight per lane before it shuffles and stores them, and writes the wire
+  // with evict-first stores.  Measured on GB300 at 128 MiB per rank (graph
+  // replay, data rotating above 2x L2): 46.8 us with one load in flight and
+  // plain stores, 45.7 us with two loads, 44.8 us with two loads and
+  // evict-first stores, 53.8 us with four loads.  The same change made an
+  // L2-resident 1 MiB encode 9 % slower (its wire is read from L2 by the next
+  // decode) and the misaligned instance 16-47 % slower, so they keep one
+  // iteration and plain stores.
+  constexpr int kEncodeUnroll = kStream ? 2 : 1;
+  for (int64_t wp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp0 < pairs;
+       wp0 += kEncodeUnroll * nwarps) {
+    uint4 d[kEncodeUnroll];
+#pragma unroll
+    for (int u = 0; u < kEncodeUnroll; u++) {
+      const int64_t p = 2 * (wp0 + u * nwarps) + (lane >> 4);
+      d[u] = make_uint4(0u, 0u, 0u, 0u);
+      const int64_t doff = p * 240 + 16 * c;
+      if (!kMis) {
+        if (p < pairs && c < 15 && doff < data_bytes) d[u] = ld_stream(data + doff);
+      } else {
+        const int m = (int)(reinterpret_cast<uintptr_t>(data) & 15u);
+        uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+        if (p < pairs && doff - m < data_bytes) blk = ld_stream(data - m + doff);
+        const uint4 nxt = shfl_down16(blk, 1, 16);
+        if (p < pairs && c < 15 && doff < data_bytes) d[u] = bytes_at(blk, nxt, m);
+      }
     }
-    const uint64_t x = lo64(d), y = hi64(d);
-    const uint64_t y_prev = __shfl_up_sync(kFull, y, 1, 16);
-    const uint64_t first = c <= 7 ? x : y_prev;
-    const uint64_t second = c <= 6 ? y : ((c == 7 || c == 15) ? flag : x);
-    const int64_t line = 2 * p + (c >> 3);
-    if (p < pairs && line < lines) st16(wire + p * 256 + 16 * c, make16(first, second));
+#pragma unroll
+    for (int u = 0; u < kEncodeUnroll; u++) {
+      const int64_t p = 2 * (wp0 + u * nwarps) + (lane >> 4);
+      const uint64_t x = lo64(d[u]), y = hi64(d[u]);
+      const uint64_t y_prev = __shfl_up_sync(kFull, y, 1, 16);
+      const uint64_t first = c <= 7 ? x : y_prev;
+      const uint64_t second = c <= 6 ? y : ((c == 7 || c == 15) ? flag : x);
+      const int64_t line = 2 * p + (c >> 3);
+      if (p < pairs && line < lines) {
+        if (kStream)
+          st16_evict_first(wire + p * 256 + 16 * c, make16(first, second));
+        else
+          st16(wire + p * 256 + 16 * c, make16(first, second));
+      }
+    }
   }
 }
 
@@ -245,21 +279,29 @@ DecodeFn pick_decode(int dtype, int W, bool mis = false) {
   }
 }
 
+using EncodeFn = void (*)(const uint8_t*, const int64_t, const int64_t, const uint64_t, uint8_t*);
+
+EncodeFn pick_encode(bool mis, int64_t lines) {
+  if (mis) return ll128_encode_kernel<true, false>;
+  return 128 * lines >= kStreamWireBytes ? ll128_encode_kernel<false, true> : ll128_encode_kernel<false, false>;
+}
+
 }  // namespace
 
-cudaError_t ll128_occupancy(int dtype, int W, bool mis, int* decode_blocks_per_sm, int* encode_blocks_per_sm) {
+cudaError_t ll128_occupancy(int dtype, int W, bool mis, int64_t lines, int* decode_blocks_per_sm,
+                            int* encode_blocks_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W, mis)), kWireThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       encode_blocks_per_sm,
-      reinterpret_cast<const void*>(mis ? ll128_encode_kernel<true> : ll128_encode_kernel<false>), kWireThreads, 0);
+      reinterpret_cast<const void*>(pick_encode(mis, lines)), kWireThreads, 0);
 }
 
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
                                 void* wire, int grid, cudaStream_t s) {
   const bool mis = (reinterpret_cast<uintptr_t>(data) & 15u) != 0;
-  return launch_pdl(mis ? ll128_encode_kernel<true> : ll128_encode_kernel<false>, (unsigned)grid, kWireThreads, 0,
+  return launch_pdl(pick_encode(mis, lines), (unsigned)grid, kWireThreads, 0,
                     s, 1, static_cast<const uint8_t*>(data), data_bytes, lines, flag, static_cast<uint8_t*>(wire));
 }
 

@@ -134,7 +134,7 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
     int& per_sm = st->per_sm[dtype][w_instance(W)][mis ? 1 : 0];
     if (per_sm == 0) {
       int enc = 0;
-      e = ll128_occupancy(dtype, W, mis, &per_sm, &enc);
+      e = ll128_occupancy(dtype, W, mis, lines, &per_sm, &enc);
       if (e != cudaSuccess) {
         per_sm = 0;
         return cuda_error(e, "ll128 occupancy");
