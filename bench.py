@@ -240,7 +240,9 @@ def hold_device():
     blocking-kernel technique of GPU benchmark suites)."""
     import torch
 
-    torch.cuda._sleep(int(HOLD_NS * 2.1))   # clock cycles at about 2.1 GHz
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:   # without it the region also holds the host's submission latency
+        sleep(int(HOLD_NS * 2.1))   # clock cycles at about 2.1 GHz
 
 
 def capture(torch, launches):
