@@ -620,6 +620,61 @@ def test_chained_calls_see_previous_outputs(car, M):
         ref_res, ref_x0 = ref_ro, ref_ar
 
 
+@pytest.mark.parametrize("M", [400, 700])
+def test_chained_pipeline_calls_see_previous_outputs(car, M):
+    """The pipelined fused kernel (more rows than SMs, 16 KB rows) behind a
+    predecessor that writes its inputs: a plain reduce whose output is rank 0
+    of the first fused call, then fused calls whose residual and rank 0 are
+    the previous call's residual_out and ar.  Each launch may ask L2 for its
+    first row while the predecessor still runs; every call must still read
+    the predecessor's results."""
+    W, N, steps = 8, 8192, 3
+    wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=960 + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    first = torch.full_like(dx[0], float("nan"))
+    outs = [(torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)) for _ in range(steps)]
+    with car.Car(W, M, N, "bf16") as c:
+        c.reduce(dx, first)
+        cur_res, cur_x0 = dres, first
+        for k in range(steps):
+            ro, no, ar = outs[k]
+            c.reduce_residual_rmsnorm([cur_x0] + dx[1:], cur_res, dw, wl.eps, ro, no, ar)
+            cur_res, cur_x0 = ro, ar
+        c.sync()
+    torch.cuda.synchronize()
+    ref_res, ref_x0 = res, oracle_reduce(xs, "bf16")
+    assert_bits_equal(first, ref_x0, "reduce before the chain")
+    for k in range(steps):
+        ref_ar, ref_ro, ref_no = oracle_fused([ref_x0] + xs[1:], ref_res, w, wl.eps, M, N, "bf16")
+        ro, no, ar = outs[k]
+        assert_bits_equal(ar, ref_ar, f"ar step {k}")
+        assert_bits_equal(ro, ref_ro, f"residual_out step {k}")
+        assert_norm_close(no, ref_no, f"norm_out step {k}")
+        ref_res, ref_x0 = ref_ro, ref_ar
+
+
+@pytest.mark.parametrize("M", [1919, 1920, 1921])
+def test_ll128_encode_on_both_sides_of_the_streaming_size(car, M):
+    """Aligned rank data whose wire reaches 32 MiB is encoded by the
+    streaming instance (two loads in flight, evict-first stores), smaller
+    data by the plain one: wires bit-identical to the oracle's below, at and
+    above that size (N=8192 bf16; M=1921 ends in a partial line)."""
+    N = 8192
+    wl = workloads.custom(1, M, N, "bf16", seed=970 + M)
+    x = workloads.make_x(wl, 0)
+    D = wl.data_bytes
+    with car.Car(1, M, N, "bf16") as c:
+        wire = torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=DEV)
+        c.ll128_encode(x.to(DEV), 7, wire)
+        torch.cuda.synchronize()
+        assert (c.ll128_wire_bytes >= 32 << 20) == (M >= 1920)
+    want = np.empty(oracle.ll128_wire_bytes(D), dtype=np.uint8)
+    oracle.ll128_encode(x.view(-1).view(torch.uint8).numpy(), D, 7, want)
+    got = wire.cpu().numpy()
+    assert np.array_equal(got, want), f"first differing byte {int(np.nonzero(got != want)[0][0])}"
+
+
 @pytest.mark.parametrize("kind", ["one_shot", "two_shot"])
 @pytest.mark.parametrize("W,M,N", [(4, 33, 1032), (8, 512, 8192)])
 def test_chained_reduces_see_previous_output(car, kind, W, M, N):
