@@ -190,7 +190,13 @@ car_status car_ll128_decode_reduce(car_ctx* h, const void* const* wires, uint64_
 
 /* Wait for the stream of the last car_ll128_decode_reduce on this handle and
  * fill *out.  Returns CAR_ERR_STALE_FLAG when n_stale > 0, CAR_OK when none
- * (or when no decode has run), CAR_ERR_HANDLE / CAR_ERR_ARG / CAR_ERR_CUDA. */
+ * (or when no decode has run), CAR_ERR_HANDLE / CAR_ERR_ARG / CAR_ERR_CUDA.
+ * Reading the report clears its count: a decode captured in a CUDA graph and
+ * replayed reports each replay's stale lines when the report follows each
+ * replay (replays without a report in between add up), and a second report
+ * with no decode in between finds none.  The report waits only for the stream
+ * the decode was issued (or captured) on: after a graph replay on another
+ * stream, wait for that stream first. */
 car_status car_ll128_report(car_ctx* h, car_stale_report* out);
 
 /* Allocation-free variant of car_ll128_decode_reduce.  The pages have no

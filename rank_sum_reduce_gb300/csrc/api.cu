@@ -264,6 +264,14 @@ car_status report_common(car_ctx* h, int which, car_stale_report* out) {
                    cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "read stale list");
   }
+  // Clear the count just read.  A decode zeroes only the other slot (for the
+  // call after it), so a single decode captured in a CUDA graph would
+  // otherwise add every replay's stale lines to the same count.
+  if (n) {
+    e = cudaMemsetAsync(&h->log[which]->n[h->last_slot[which]], 0, sizeof(n), h->last_stream[which]);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->last_stream[which]);
+    if (e != cudaSuccess) return cuda_fail(e, "clear stale count");
+  }
   out->n_stale = n;
   out->n_listed = (uint32_t)listed;
   return n ? CAR_ERR_STALE_FLAG : CAR_OK;

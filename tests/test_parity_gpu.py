@@ -702,6 +702,53 @@ def test_chained_reduces_see_previous_output(car, kind, W, M, N):
         ref = want
 
 
+@pytest.mark.parametrize("fmt", ["ll128", "ll"])
+def test_graph_of_one_decode_reports_each_replay(car, fmt):
+    """One decode captured in a CUDA graph: every replay, followed by a
+    report, reports exactly the stale lines planted for that replay, and the
+    output equals the oracle's decode of the same wires."""
+    W, M, N = 3, 5, 1000
+    wl = workloads.custom(W, M, N, "bf16", seed=1500)
+    xs = [workloads.make_x(wl, r) for r in range(W)]
+    D = wl.data_bytes
+    lb = 128 if fmt == "ll128" else 16
+    off = 120 if fmt == "ll128" else 4                   # the flag word (LL: flag1)
+    with car.Car(W, M, N, "bf16") as c:
+        nb = c.ll128_wire_bytes if fmt == "ll128" else c.ll_wire_bytes
+        wires = [torch.empty(nb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+        enc = c.ll128_encode if fmt == "ll128" else c.ll_encode
+        dec = c.ll128_decode_reduce if fmt == "ll128" else c.ll_decode_reduce
+        rep = c.ll128_report if fmt == "ll128" else c.ll_report
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            dec(wires, 9, out, stream=side.cuda_stream)
+            side.synchronize()
+            rep()
+            with torch.cuda.graph(g, stream=side):
+                dec(wires, 9, out, stream=torch.cuda.current_stream().cuda_stream)
+        L = nb // lb
+        for trial, plan in enumerate(({0: [1, 7]}, {2: [0], 1: [L - 1, 3]}, {})):
+            for x, wv in zip(xs, wires):
+                enc(x.to(DEV), 9, wv)
+            for r, ks in plan.items():
+                for k in ks:
+                    wires[r][k * lb + off] ^= 0x01
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()                       # the report waits only for the capture stream
+            n, pairs = rep()
+            planted = {(r, k) for r, ks in plan.items() for k in ks}
+            assert n == len(planted) and set(pairs) == planted, f"replay {trial}"
+            host = [wv.cpu().numpy() for wv in wires]
+            ref = torch.empty_like(xs[0])
+            (oracle.ll128_decode_reduce if fmt == "ll128" else oracle.ll_decode_reduce)(host, D, "bf16", 9, ref)
+            assert_bits_equal(out, ref, f"{fmt} decode (replay {trial})")
+        assert rep()[0] == 0                               # the report cleared what it returned
+        del g
+
+
 @pytest.mark.parametrize("M", [1, 400])
 def test_graph_capture_replays_correctly(car, M):
     """Capture reduce + fused + LL128 encode/decode in one CUDA graph, change
