@@ -208,8 +208,8 @@ car_status car_ll128_report(car_ctx* h, car_stale_report* out);
  * synchronisation an allocation or free can cause.
  *
  * It needs no handle and allocates nothing.  Its stale-line log is a fixed
- * device array inside the library (CAR_STALE_LIST_MAX pairs, 512 KiB plus a
- * 16-byte count) that every GPU which loads the library keeps until the
+ * device array inside the library (CAR_STALE_LIST_MAX pairs, 512 KiB plus
+ * two 8-byte counts) that every GPU which loads the library keeps until the
  * process exits.  The first call on a device looks up that array's device
  * address and the device's SM count, with the device current; make that
  * first call before any stream capture on the device.  The address is kept
@@ -217,16 +217,12 @@ car_status car_ll128_report(car_ctx* h, car_stale_report* out);
  * (cudaDeviceReset) after that first call: a reset can place the array
  * elsewhere, and the kept address would then point at other memory.
  *
- * Cost against the handle path: a memset before the kernel (the count) and a
- * device-to-device copy after it (the report).  Neither is a kernel, so
- * programmatic dependent launch cannot overlap this call with its
- * neighbours in the stream.
- *
- * Every call on a device shares the array and it keeps the last call's
- * contents.  Each call clears the count on `stream` before its launch, so
- * calls queued one after another on one stream are fine; calls that overlap
- * on the GPU (two streams at once) race on the array and their reports are
- * wrong.
+ * Each call is one kernel launch.  The last of its CTAs to finish copies the
+ * report into stale_out and clears the array's counts for the next call, so
+ * calls queued one after another on one stream (or replayed from a CUDA
+ * graph) each report their own stale lines.  Every call on a device shares
+ * the array: calls that overlap on the GPU (two streams at once) race on it
+ * and their reports are wrong.
  *
  * Arguments: the shape (W, M, N, dtype) and data as for car_create and
  * car_ll128_decode_reduce (wires: W dev pointers of 128*ceil(M*N*s/120)

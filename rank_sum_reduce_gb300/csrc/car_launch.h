@@ -73,13 +73,18 @@ constexpr int kWireThreads = 256;
 // Resident CTAs per SM of the decode and encode instances that a call with
 // 16-byte aligned (mis = false) or misaligned (mis = true) output / rank data
 // launches on a message of `lines` LL128 lines.
+// publish: the decode instance of the allocation-free entry (see ll128.cu).
 cudaError_t ll128_occupancy(int dtype, int W, bool mis, int64_t lines, int* decode_blocks_per_sm,
-                            int* encode_blocks_per_sm);
+                            int* encode_blocks_per_sm, bool publish = false);
 cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t lines, uint64_t flag,
                                 void* wire, int grid, cudaStream_t s);
+// With a report buffer, the allocation-free instance: `log` is the shared
+// array (slot unused), and the last CTA writes the count and the first `cap`
+// pairs to `report` and clears the array.
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
-                                       StaleLog* log, int log_slot, int grid, cudaStream_t s);
+                                       StaleLog* log, int log_slot, int grid, cudaStream_t s,
+                                       void* report = nullptr, uint32_t cap = 0);
 
 // ---- Lamport one-shot push, bf16 (lamport.cu) ----
 bool lamport_has_variant(int W, int vpt);

@@ -143,11 +143,47 @@ __global__ void __launch_bounds__(kWireThreads)
 // and b; the blocks inside the warp's range are stored whole, the first and
 // last (shared with the neighbouring warps) and any block past the end of the
 // data are stored 2 bytes at a time, only over the bytes this warp owns.
-template <int DT, int W, bool kMisOut>
+// Allocation-free calls (kPublish): the log is one array that every call on
+// the device shares, with n[0] the stale count and n[1] a count of finished
+// CTAs.  The last CTA to finish copies the count and the first `cap` pairs
+// into the caller's report (uint64 count, 8 reserved bytes, uint32 pairs)
+// and clears both counts for the next call, which waits for this grid before
+// it logs.  So a call is one kernel: no memset before it and no copy after it
+// that would keep programmatic dependent launch from overlapping its
+// neighbours.
+__device__ __forceinline__ void publish_report(StaleLog* log, uint8_t* report, uint32_t cap) {
+  __shared__ unsigned int s_last;
+  __syncthreads();  // every stale entry of this CTA is written
+  if (threadIdx.x == 0) {
+    __threadfence();  // ... and visible to the whole GPU before this CTA counts as finished
+    const unsigned long long done = atomicAdd(&log->n[1], 1ull);
+    s_last = done == (unsigned long long)gridDim.x - 1ull ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const unsigned long long count = *reinterpret_cast<volatile unsigned long long*>(&log->n[0]);
+  const uint32_t listed = count < (unsigned long long)cap ? (uint32_t)count : cap;
+  unsigned long long* dst = reinterpret_cast<unsigned long long*>(report);
+  if (threadIdx.x == 0) {
+    dst[0] = count;
+    dst[1] = 0ull;
+  }
+  const volatile unsigned long long* pairs = reinterpret_cast<const volatile unsigned long long*>(&log->entry[0][0]);
+  for (uint32_t i = threadIdx.x; i < listed; i += blockDim.x) dst[2 + i] = pairs[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    log->n[0] = 0ull;
+    log->n[1] = 0ull;
+  }
+}
+
+template <int DT, int W, bool kMisOut, bool kPublish>
 __global__ void __launch_bounds__(kWireThreads)
     ll128_decode_reduce_kernel(const RankPtrs wires, const int nranks, const int64_t data_bytes,
                                const int64_t lines, const uint64_t expected, const int max_polls,
-                               uint8_t* __restrict__ out, StaleLog* __restrict__ log, const int slot) {
+                               uint8_t* __restrict__ out, StaleLog* __restrict__ log, const int slot,
+                               uint8_t* __restrict__ report, const uint32_t cap) {
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : nranks;
   const int lane = threadIdx.x & 31, c = lane & 15;
@@ -169,7 +205,7 @@ __global__ void __launch_bounds__(kWireThreads)
     }
   }
   pdl_wait_and_release();
-  prepare_next_log(log, slot);
+  if (!kPublish) prepare_next_log(log, slot);
   for (int64_t wp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * wp < pairs;
        wp += nwarps) {
     const int64_t p = 2 * wp + (lane >> 4);
@@ -255,27 +291,34 @@ __global__ void __launch_bounds__(kWireThreads)
       }
     }
   }
+  if (kPublish) publish_report(log, report, cap);
 }
 
 using DecodeFn = void (*)(const RankPtrs, const int, const int64_t, const int64_t, const uint64_t,
-                          const int, uint8_t*, StaleLog*, const int);
+                          const int, uint8_t*, StaleLog*, const int, uint8_t*, const uint32_t);
 
-template <int DT, bool kMis>
+template <int DT, bool kMis, bool kPub>
 DecodeFn pick_dt(int W) {
   switch (W) {
-    case 2: return ll128_decode_reduce_kernel<DT, 2, kMis>;
-    case 4: return ll128_decode_reduce_kernel<DT, 4, kMis>;
-    case 8: return ll128_decode_reduce_kernel<DT, 8, kMis>;
-    case 16: return ll128_decode_reduce_kernel<DT, 16, kMis>;
-    default: return ll128_decode_reduce_kernel<DT, 0, kMis>;
+    case 2: return ll128_decode_reduce_kernel<DT, 2, kMis, kPub>;
+    case 4: return ll128_decode_reduce_kernel<DT, 4, kMis, kPub>;
+    case 8: return ll128_decode_reduce_kernel<DT, 8, kMis, kPub>;
+    case 16: return ll128_decode_reduce_kernel<DT, 16, kMis, kPub>;
+    default: return ll128_decode_reduce_kernel<DT, 0, kMis, kPub>;
   }
 }
 
-DecodeFn pick_decode(int dtype, int W, bool mis = false) {
+template <int DT>
+DecodeFn pick_dt(int W, bool mis, bool publish) {
+  if (publish) return mis ? pick_dt<DT, true, true>(W) : pick_dt<DT, false, true>(W);
+  return mis ? pick_dt<DT, true, false>(W) : pick_dt<DT, false, false>(W);
+}
+
+DecodeFn pick_decode(int dtype, int W, bool mis, bool publish) {
   switch (dtype) {
-    case kBF16: return mis ? pick_dt<kBF16, true>(W) : pick_dt<kBF16, false>(W);
-    case kFP16: return mis ? pick_dt<kFP16, true>(W) : pick_dt<kFP16, false>(W);
-    default: return mis ? pick_dt<kFP32, true>(W) : pick_dt<kFP32, false>(W);
+    case kBF16: return pick_dt<kBF16>(W, mis, publish);
+    case kFP16: return pick_dt<kFP16>(W, mis, publish);
+    default: return pick_dt<kFP32>(W, mis, publish);
   }
 }
 
@@ -289,9 +332,9 @@ EncodeFn pick_encode(bool mis, int64_t lines) {
 }  // namespace
 
 cudaError_t ll128_occupancy(int dtype, int W, bool mis, int64_t lines, int* decode_blocks_per_sm,
-                            int* encode_blocks_per_sm) {
+                            int* encode_blocks_per_sm, bool publish) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W, mis)), kWireThreads, 0);
+      decode_blocks_per_sm, reinterpret_cast<const void*>(pick_decode(dtype, W, mis, publish)), kWireThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       encode_blocks_per_sm,
@@ -307,10 +350,12 @@ cudaError_t launch_ll128_encode(const void* data, int64_t data_bytes, int64_t li
 
 cudaError_t launch_ll128_decode_reduce(int dtype, int W, const RankPtrs& wires, int64_t data_bytes,
                                        int64_t lines, uint64_t expected, int max_polls, void* out,
-                                       StaleLog* log, int slot, int grid, cudaStream_t s) {
+                                       StaleLog* log, int slot, int grid, cudaStream_t s, void* report,
+                                       uint32_t cap) {
   const bool mis = (reinterpret_cast<uintptr_t>(out) & 15u) != 0;
-  return launch_pdl(pick_decode(dtype, W, mis), (unsigned)grid, kWireThreads, 0, s, 1, wires, W, data_bytes, lines,
-                    expected, max_polls, static_cast<uint8_t*>(out), log, slot);
+  return launch_pdl(pick_decode(dtype, W, mis, report != nullptr), (unsigned)grid, kWireThreads, 0, s, 1, wires, W,
+                    data_bytes, lines, expected, max_polls, static_cast<uint8_t*>(out), log, slot,
+                    static_cast<uint8_t*>(report), cap);
 }
 
 }  // namespace car

@@ -10,10 +10,12 @@
 // handle: its stale-line log lives in a fixed device array that the library
 // itself carries (the array below), so no call allocates.
 //
-// The array is process-wide and per device: every call on a device shares it
-// and it keeps the last call's contents.  The counter is cleared on the
-// caller's stream before each launch; calls that overlap on the GPU (for
-// example on two streams at once) race on it and corrupt each other's report.
+// The array is process-wide and per device: every call on a device shares it.
+// Each call is a single kernel whose last CTA to finish copies the report to
+// the caller's buffer and clears the array's two counts for the next call;
+// the stale pairs themselves stay until the next call overwrites them.  Calls
+// that overlap on the GPU (for example on two streams at once) race on it and
+// corrupt each other's report.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -27,8 +29,9 @@
 namespace car {
 namespace {
 
-// The stale-line log of this entry point: a count followed by up to
-// kStaleCap (rank, line) pairs, laid out exactly as StaleLog.
+// The stale-line log of this entry point, laid out as StaleLog: the stale
+// count, a count of finished CTAs, then up to kStaleCap (rank, line) pairs.
+// Zero when the library is loaded, and cleared again by every call.
 constexpr size_t kScratchWords = sizeof(StaleLog) / sizeof(unsigned long long);
 static_assert(sizeof(StaleLog) % sizeof(unsigned long long) == 0, "StaleLog size");
 static __device__ __align__(256) unsigned long long g_noalloc_scratch[kScratchWords];
@@ -134,7 +137,7 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
     int& per_sm = st->per_sm[dtype][w_instance(W)][mis ? 1 : 0];
     if (per_sm == 0) {
       int enc = 0;
-      e = ll128_occupancy(dtype, W, mis, lines, &per_sm, &enc);
+      e = ll128_occupancy(dtype, W, mis, lines, &per_sm, &enc, true);
       if (e != cudaSuccess) {
         per_sm = 0;
         return cuda_error(e, "ll128 occupancy");
@@ -146,14 +149,10 @@ extern "C" car_status car_ll128_decode_reduce_noalloc(int W, int64_t M, int64_t 
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)per_sm * st->num_sms));
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  StaleLog* log = st->log;
-  e = cudaMemsetAsync(&log->n[0], 0, sizeof(log->n[0]), s);  // the count starts at zero every call
-  if (e != cudaSuccess) return cuda_error(e, "clear noalloc stale count");
-  e = launch_ll128_decode_reduce(dtype, W, tbl, D, lines, expected_flag, max_polls, ar_out, log, 0, grid, s);
+  // One kernel: its last CTA writes the report and clears the array for the
+  // next call (see publish_report in ll128.cu).
+  e = launch_ll128_decode_reduce(dtype, W, tbl, D, lines, expected_flag, max_polls, ar_out, st->log, 0, grid, s,
+                                 stale_out, cap);
   if (e != cudaSuccess) return cuda_error(e, "ll128_decode_reduce launch (noalloc)");
-  // publish the count and the first `cap` pairs to the caller's buffer
-  const size_t bytes = 2 * sizeof(unsigned long long) + (size_t)cap * 2 * sizeof(uint32_t);
-  e = cudaMemcpyAsync(stale_out, log, bytes, cudaMemcpyDeviceToDevice, s);
-  if (e != cudaSuccess) return cuda_error(e, "copy noalloc stale report");
   return CAR_OK;
 }

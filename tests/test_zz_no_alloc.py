@@ -205,3 +205,50 @@ def test_noalloc_fp32_sixteen_ranks_matches_handle_and_oracle(car):
             n_or, lst = oracle.ll128_decode_reduce(host_w, D, "fp32", 7, ref)
             assert n_or == len(planted) and {tuple(int(v) for v in e) for e in lst.tolist()} == planted
             assert np.array_equal(got, ref)
+
+
+def test_noalloc_call_replayed_from_a_cuda_graph(car):
+    """One allocation-free call captured in a CUDA graph (after a first call
+    outside capture, which sets the device up): each replay reports exactly
+    the stale lines planted for it, and its output equals the handle path's."""
+    dev = "cuda:0"
+    W, M, N, cap = 4, 7, 1000, 32
+    wl = workloads.custom(W, M, N, "bf16", seed=606)
+    xs = [workloads.make_x(wl, r, dev) for r in range(W)]
+    L = oracle.ll128_lines(wl.data_bytes)
+    with car.Car(W, M, N, "bf16") as handle:
+        wires = [torch.empty(handle.ll128_wire_bytes, dtype=torch.uint8, device=dev) for _ in range(W)]
+        out_na = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        out_ref = torch.empty_like(out_na)
+        stale_buf = torch.zeros(16 + 8 * cap, dtype=torch.uint8, device=dev)
+        ptrs = [w.data_ptr() for w in wires]
+        side = torch.cuda.Stream()
+
+        def call(stream):
+            st = car.car_ll128_decode_reduce_noalloc(W, M, N, car.CAR_BF16, ptrs, 7, 1, out_na.data_ptr(),
+                                                     stale_buf.data_ptr(), cap, stream)
+            assert st == car.CAR_OK, car.car_last_error()
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            call(side.cuda_stream)
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                call(torch.cuda.current_stream().cuda_stream)
+        old = torch.tensor(list((6).to_bytes(8, "little")), dtype=torch.uint8, device=dev)
+        for plan in ({1: [0, L - 1], 3: [2]}, {0: [5]}, {}):
+            for x, wv in zip(xs, wires):
+                handle.ll128_encode(x, 7, wv)
+            for r, ks in plan.items():
+                for k in ks:
+                    wires[r].view(L, 16, 8)[k, 15].copy_(old)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            n_na, pairs_na = _read_report(stale_buf, cap)
+            handle.ll128_decode_reduce(wires, 7, out_ref)
+            n_ref, pairs_ref = handle.ll128_report()
+            planted = {(r, k) for r, ks in plan.items() for k in ks}
+            assert n_na == n_ref == len(planted) and pairs_na == set(pairs_ref) == planted
+            assert torch.equal(out_na.view(torch.int16), out_ref.view(torch.int16))
+        del g
