@@ -942,6 +942,10 @@ PROFILE_CASES = {
     # the headline kernels on the headline workload, rotating over 4 input sets (384 MiB)
     "fused_m512_w8": (8, 512, 8192, "bf16"),
     "reduce_m512_w8": (8, 512, 8192, "bf16"),
+    # the fused row kernel at one of the page's latency-table shapes, rotating over 24 sets (353 MB)
+    "fused_rows_m128_w4": (4, 128, 8192, "bf16"),
+    # LL128 encode of one rank of the W=16 workload (134 MB of data, 143 MB of wire per launch)
+    "ll128_encode_w16": (16, 8192, 8192, "bf16"),
 }
 
 
@@ -968,6 +972,27 @@ def profile_case(name, launches=4):
             torch.cuda.synchronize()
             c.sync()
         print(f"profile case {name}: {wl.name}, {launches} launches over 4 input sets")
+        return
+    if name == "fused_rows_m128_w4":
+        wl = workloads.custom(W, M, N, dt, seed=90)
+        sets = make_sets(torch, wl, dev, 24, outputs=("ro", "no"))
+        with car.Car(W, M, N, dt) as c:
+            for i in range(launches):
+                S = sets[i % 24]
+                c.reduce_residual_rmsnorm(S["xs"], S["res"], S["w"], wl.eps, S["ro"], S["no"])
+            torch.cuda.synchronize()
+            c.sync()
+        print(f"profile case {name}: W={W} M={M} N={N} {dt}, {launches} launches over 24 input sets")
+        return
+    if name == "ll128_encode_w16":
+        wl = workloads.WORKLOADS["ll128_w16"]
+        xs = [workloads.make_x(wl, r, dev) for r in range(2)]
+        with car.Car(wl.W, wl.M, wl.N, wl.dtype) as c:
+            wires = [torch.empty(c.ll128_wire_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+            for i in range(launches):
+                c.ll128_encode(xs[i % 2], wl.ll128_flag, wires[i % 2])
+            torch.cuda.synchronize()
+        print(f"profile case {name}: {wl.name} rank data, {launches} encodes over 2 ranks")
         return
     wl = workloads.custom(W, M, N, dt, seed=90)
     xs = [workloads.make_x(wl, r, dev) for r in range(W)]
