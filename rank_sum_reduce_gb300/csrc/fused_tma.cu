@@ -373,11 +373,12 @@ __global__ void __launch_bounds__(544, 1) reduce_residual_rmsnorm_tma_kernel(con
   // before this one, prefetching the whole row only duplicates the first
   // copies and delays them.  Measured on GB300 at W = 8, M = 512, N = 8192
   // bf16 (cold launch: median of 24 ncu launches with caches flushed; step:
-  // plain reduce then this kernel, graph replay): whole row always 18.03 us
-  // cold, 25.97 us per step; none 17.07 us in graph replay of this kernel
-  // alone (against 14.65 with the prefetch); the whole row after a 100 ns
-  // grace 17.34 cold, 25.68 per step; two slices at once and the rest after
-  // the grace 17.18 cold, 25.54 per step (same box).  griddepcontrol.wait
+  // plain reduce then this kernel, graph replay).  On one box: whole row
+  // always 18.03 us cold and 25.97 us per step, whole row after a 100 ns
+  // grace 17.41 and 26.00.  On another: whole row after the grace 17.34 and
+  // 25.68, two slices at once and the rest after the grace 17.18 and 25.54.
+  // No prefetch at all: 17.07 us in graph replay of this kernel alone,
+  // against 14.65 with it.  griddepcontrol.wait
   // holds the whole warp that executes it, so thread 0 (consumer warp 0)
   // waits and sets s_dep, and no lane of the producer warp waits before the
   // warp has decided.
