@@ -39,6 +39,8 @@ import workloads  # noqa: E402
 # most steps in one timed CUDA graph, and launches per per-kernel graph (see headline)
 MAX_GRAPH_STEPS = 1024
 GRAPH_LAUNCHES = 128
+# input sets the headline step and its per-kernel graphs rotate over (see headline)
+HEADLINE_SETS = 8
 # device time (ns) of the hold kernel queued ahead of a start event (see hold_device)
 HOLD_NS = 30000
 # steps of the end-to-end measurement run on this many streams in turn, so
@@ -275,7 +277,11 @@ def headline(arm, wl, steps, warmup, rank, world):
     keep host launch overhead out of the device timeline."""
     torch, car, lib = arm.torch, arm.car, arm.lib
     set_bytes = (wl.W + 1) * wl.data_bytes + 3 * wl.data_bytes
-    R = n_sets_for(set_bytes)
+    # At least HEADLINE_SETS sets: with 4 sets of 96 MiB a graph of plain
+    # reduces alone found part of its inputs still in L2 (11.46 us per launch
+    # against 12.39-12.55 us with 5, 6 or 8 sets), although the step itself
+    # measured the same with 4, 5 and 8 sets (25.52, 25.52, 25.62 us).
+    R = max(n_sets_for(set_bytes), HEADLINE_SETS)
     sets = make_sets(torch, wl, arm.dev, R)
     st, h = car.car_create(wl.W, wl.M, wl.N, car.DTYPE_CODE[wl.dtype])
     car.check(st, "car_create")
