@@ -299,14 +299,24 @@ def test_fused_degenerate_rows(car, kernel, M, eps):
     assert_norm_close(got[keep], ref[keep])
 
 
-def test_fused_aliasing_and_no_ar(car):
-    W, M, N = 4, 6, 2048
-    wl, xs, res, w = _fused_inputs(W, M, N, "bf16", seed=31)
-    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, "bf16")
+@pytest.mark.parametrize("W,M,N,dtype,kernel", [
+    (4, 6, 2048, "bf16", "rows"),
+    (8, 400, 8192, "bf16", "pipeline"),   # ranks 6, 7 and the residual loaded by the consumers
+    (8, 400, 8192, "bf16", "pipeline_w7"),  # ar_out == the last rank, a register-loaded slice
+    (4, 333, 4096, "fp32", "pipeline"),   # every slice through the bulk-copy ring
+])
+def test_fused_aliasing_and_no_ar(car, W, M, N, dtype, kernel):
+    """residual_out == residual, and ar_out == one rank's input: each element
+    is read before the same CTA writes it."""
+    wl, xs, res, w = _fused_inputs(W, M, N, dtype, seed=31 + M)
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, dtype)
+    tune = car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE
+    k = W - 1 if kernel == "pipeline_w7" else 2
     dx = [x.to(DEV) for x in xs]
     dres, dw = res.to(DEV), w.to(DEV)
     no = torch.empty_like(dres)
-    with car.Car(W, M, N, "bf16") as c:
+    with car.Car(W, M, N, dtype) as c:
+        c.tune_fused(tune)
         c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, dres, no, None)   # residual_out == residual
     torch.cuda.synchronize()
     assert_bits_equal(dres, ref_ro, "residual_out in place")
@@ -314,11 +324,13 @@ def test_fused_aliasing_and_no_ar(car):
     dx = [x.to(DEV) for x in xs]
     dres = res.to(DEV)
     ro = torch.empty_like(dres)
-    with car.Car(W, M, N, "bf16") as c:
-        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, dx[2])   # ar_out == inputs[2]
+    with car.Car(W, M, N, dtype) as c:
+        c.tune_fused(tune)
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, dx[k])   # ar_out == inputs[k]
     torch.cuda.synchronize()
-    assert_bits_equal(dx[2], ref_ar, "ar in place")
+    assert_bits_equal(dx[k], ref_ar, "ar in place")
     assert_bits_equal(ro, ref_ro, "residual_out")
+    assert_norm_close(no, ref_no)
 
 
 def test_fused_rejects_rows_beyond_limit(car):
