@@ -153,9 +153,10 @@ __global__ void __launch_bounds__(kWireThreads)
 // neighbours.
 __device__ __forceinline__ void publish_report(StaleLog* log, uint8_t* report, uint32_t cap) {
   __shared__ unsigned int s_last;
-  __syncthreads();  // every stale entry of this CTA is written
+  __threadfence();  // this thread's stale entries are visible to the whole GPU
+  __syncthreads();  // ... for every thread of the CTA
   if (threadIdx.x == 0) {
-    __threadfence();  // ... and visible to the whole GPU before this CTA counts as finished
+    __threadfence();
     const unsigned long long done = atomicAdd(&log->n[1], 1ull);
     s_last = done == (unsigned long long)gridDim.x - 1ull ? 1u : 0u;
   }
