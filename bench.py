@@ -511,9 +511,11 @@ def isolated_latency(arm, wl, outputs, calls=200, n_sets=4):
     flushed (a read of twice its size), a hold kernel is queued, then the
     start event, one CUDA-graph replay holding one call (buffer sets
     rotating), and the end event.  Returns the median and the 95th percentile
-    in us, the samples' minimum and maximum, and the median of the same
-    sequence with nothing between the two events (what the event pair itself
-    costs on the device)."""
+    in us, the samples' minimum and maximum, the same two figures for the
+    C-ABI call launched straight onto the stream instead of through a graph
+    (`direct_*`; the hold kernel covers the host's time in the call), and the
+    median of the same sequence with nothing between the two events (what
+    the event pair itself costs on the device)."""
     torch, car = arm.torch, arm.car
     sets = make_sets(torch, wl, arm.dev, n_sets, outputs=("ar", "ro", "no"))
     c = car.Car(wl.W, wl.M, wl.N, wl.dtype)
@@ -530,31 +532,39 @@ def isolated_latency(arm, wl, outputs, calls=200, n_sets=4):
                 raise RuntimeError(car.car_last_error())
         return run
 
-    graphs = [capture(torch, [call_fn(S)]) for S in sets]
+    fns = [call_fn(S) for S in sets]
+    graphs = [capture(torch, [f]) for f in fns]
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=arm.dev)
     cs = torch.cuda.current_stream()
 
-    def sample(with_call):
+    def sample(kind):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
         torch.cuda.synchronize()
         for i, (a, b) in enumerate(evs):
             flush.sum()
             hold_device()
             a.record(cs)
-            if with_call:
+            if kind == "graph":
                 graphs[i % n_sets].replay()
+            elif kind == "direct":
+                fns[i % n_sets](cs.cuda_stream)
             b.record(cs)
         torch.cuda.synchronize()
         return sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
 
-    us = sample(True)
-    empty = sample(False)   # the same sequence with nothing between the events
+    def p95(v):
+        return v[min(len(v) - 1, int(0.95 * len(v)))]
+
+    us = sample("graph")
+    direct = sample("direct")
+    empty = sample("none")   # the same sequence with nothing between the events
     c.sync()   # raises if a bounded wait ran out
     del graphs, flush
     c.close()
     med = statistics.median(us)
-    return {"median_us": round(med, 3), "p95_us": round(us[min(len(us) - 1, int(0.95 * len(us)))], 3),
+    return {"median_us": round(med, 3), "p95_us": round(p95(us), 3),
             "min_us": round(us[0], 3), "max_us": round(us[-1], 3), "calls": calls,
+            "direct_median_us": round(statistics.median(direct), 3), "direct_p95_us": round(p95(direct), 3),
             "empty_event_pair_median_us": round(statistics.median(empty), 3),
             "net_median_us": round(med - statistics.median(empty), 3)}
 
@@ -1072,6 +1082,7 @@ def main():
             rows[key]["isolated"] = isolated_latency(arm, wl_m1, outputs)
             iso = rows[key]["isolated"]
             m1[name] = {"median_us": iso["median_us"], "p95_us": iso["p95_us"],
+                        "direct_median_us": iso["direct_median_us"], "direct_p95_us": iso["direct_p95_us"],
                         "empty_events_us": iso["empty_event_pair_median_us"], "b2b_us_per_call": rows[key]["us_per_call"]}
         rows["lamport_m1_w2"] = lamport_row(arm, workloads.WORKLOADS["m1_w2"])
         rows["lamport_m1_w8"] = lamport_row(arm, workloads.WORKLOADS["m1_w8"])
