@@ -6,7 +6,7 @@ synchronisation an allocation implies), so they cannot create a handle.
 car_ll128_decode_reduce_noalloc serves them with a stale-line log kept in a
 fixed device array inside the library.  This test checks, through the C ABI,
 that two calls in a row give the same output and the same stale report as
-the handle-based entry point, that the second call does not see the first
+the handle-based entry point and the oracle, that the second call does not see the first
 call's stale lines, and that the calls change no device memory use.
 
 The file is named to be collected last, so that a run stopping at the first
@@ -56,6 +56,19 @@ def _assert_no_device_memory_change(free_before, reserved_before):
     if free_after != free_before:
         others = _other_compute_processes()
         assert others, f"free device memory changed by {free_before - free_after} bytes with no other process"
+
+
+def _oracle_decode(wires, D, dtype):
+    """The oracle's decode of the wires as they are now: (stale count, stale
+    set, output bytes)."""
+    host_w = [wv.cpu().numpy() for wv in wires]
+    ref = np.empty(D, dtype=np.uint8)
+    n, lst = oracle.ll128_decode_reduce(host_w, D, dtype, 7, ref)
+    return n, {tuple(int(v) for v in e) for e in lst.tolist()}, ref
+
+
+def _bytes(t):
+    return t.contiguous().view(-1).view(torch.uint8).cpu().numpy()
 
 
 def _read_report(buf, cap):
@@ -111,16 +124,18 @@ def test_noalloc_matches_handle_path_on_two_calls(car):
         noalloc_call(7)
         torch.cuda.synchronize()
         n_na, pairs_na = _read_report(stale_buf, cap)
-        results.append((plan, n_ref, set(pairs_ref), n_na, pairs_na, out_ref.cpu(), out_na.cpu()))
+        results.append((plan, n_ref, set(pairs_ref), n_na, pairs_na, out_ref.cpu(), out_na.cpu(),
+                        _oracle_decode(wires, D, dtype)))
     torch.cuda.synchronize()
     _assert_no_device_memory_change(free_before, reserved_before)
     handle.close()
 
-    for plan, n_ref, pairs_ref, n_na, pairs_na, o_ref, o_na in results:
+    for plan, n_ref, pairs_ref, n_na, pairs_na, o_ref, o_na, (n_or, pairs_or, b_or) in results:
         planted = {(r, k) for r, ks in plan.items() for k in ks}
-        assert n_ref == n_na == len(planted)
-        assert pairs_ref == pairs_na == planted
+        assert n_ref == n_na == n_or == len(planted)
+        assert pairs_ref == pairs_na == pairs_or == planted
         assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16))
+        assert np.array_equal(_bytes(o_na), b_or)
 
 
 def test_noalloc_rejects_cap_beyond_its_array(car):
@@ -169,6 +184,8 @@ def test_noalloc_counts_every_stale_line_beyond_cap(car):
     assert n_ref == n_na == len(planted) == 5
     assert set(pairs_ref) == planted and len(pairs_na) == cap and pairs_na <= planted
     assert torch.equal(out_na.view(torch.int16), out_ref.view(torch.int16))
+    n_or, pairs_or, b_or = _oracle_decode(wires, wl.data_bytes, "bf16")
+    assert n_or == 5 and pairs_or == planted and np.array_equal(_bytes(out_na), b_or)
 
 
 def test_noalloc_fp32_sixteen_ranks_matches_handle_and_oracle(car):
@@ -251,4 +268,6 @@ def test_noalloc_call_replayed_from_a_cuda_graph(car):
             planted = {(r, k) for r, ks in plan.items() for k in ks}
             assert n_na == n_ref == len(planted) and pairs_na == set(pairs_ref) == planted
             assert torch.equal(out_na.view(torch.int16), out_ref.view(torch.int16))
+            n_or, pairs_or, b_or = _oracle_decode(wires, wl.data_bytes, "bf16")
+            assert n_or == len(planted) and pairs_or == planted and np.array_equal(_bytes(out_na), b_or)
         del g
