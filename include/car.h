@@ -348,8 +348,8 @@ car_status car_sync(car_ctx* h, void* stream);
  *
  * With cta in 0..7: the split row's partial exchange waits at most
  * wait_limit_ns (1000 .. 1e9) instead of about one second, and CTA `cta` of
- * the cluster that takes row `row` (0 .. M-1) pushes its partial delay_ns
- * (at most CAR_TEST_MAX_DELAY_NS) late.  A peer whose wait runs out first
+ * the cluster that takes row `row` (0 .. M-1) reaches that row's exchange,
+ * and so pushes its partial, delay_ns (at most CAR_TEST_MAX_DELAY_NS) late.  A peer whose wait runs out first
  * sets the handle's error flag (car_sync then returns CAR_ERR_TIMEOUT),
  * writes NaN for its columns of that row's norm_out, and then waits (bounded
  * by about one second) until the late partial has landed before it goes on,

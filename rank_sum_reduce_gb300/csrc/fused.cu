@@ -84,12 +84,13 @@ __global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
   constexpr int E = Pack<DT>::kN;
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : p.nranks;
-  __shared__ float s_warp[32];
+  __shared__ float s_warp[2][32];             // warp partials, by row parity
   __shared__ float s_part[2][8];               // the cluster's CTA partials, by row parity
   __shared__ __align__(8) uint64_t s_xbar[2];  // all C partials of the row have landed, by row parity
   __shared__ float s_total;
 
-  const int C = p.cluster;
+  // Instances held to two CTAs per SM are launched for whole rows only.
+  const int C = MINB > 1 ? 1 : p.cluster;
   const int crank = C > 1 ? (int)cluster_rank() : 0;
   const int64_t ngroups = gridDim.x / C;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -155,53 +156,64 @@ __global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
       }
     }
 
-    // 3. row statistic: warp shuffle, then shared memory across warps, then
-    //    (split rows) each CTA pushes its partial into every CTA of the
-    //    cluster (st.async, counted on the receiver's mbarrier) and adds the
-    //    C partials in rank order once they have landed: one one-way hop, and
-    //    every CTA of the row sees the same total.
+    // 3. row statistic: warp shuffle, then shared memory across warps.
+    //    One CTA per row: warp 0 adds the warp partials and broadcasts the
+    //    total through shared memory.  Split rows: every warp adds the warp
+    //    partials itself (same values, same order, so the same sum), lanes
+    //    0 .. C-1 of warp 0 push it into every CTA of the cluster (st.async,
+    //    counted on the receiver's mbarrier), and every thread waits for the
+    //    C partials and adds them in rank order: one one-way hop, no second
+    //    CTA barrier, and every CTA of the row sees the same total.  The
+    //    butterfly leaves the same sum in every lane (at each step both lanes
+    //    of a pair add the same two values, in either order, and fp32
+    //    addition commutes).  W = 8, M = 1, N = 8192: 2.01 -> 1.95 us per
+    //    call back to back; W = 16: 2.15 -> 2.08 us.  With one CTA per row
+    //    the second barrier stays: without it, many rows per CTA ran 1-2 %
+    //    slower.
     ss = warp_sum(ss);
-    if (lane == 0) s_warp[warp] = ss;
+    const uint32_t b = it & 1u;
+    if (lane == 0) s_warp[b][warp] = ss;
     if (!peers_ready) {
       cluster_wait();  // every peer's mbarriers are initialised
       peers_ready = true;
     }
+    // test hook: this whole CTA reaches the exchange late
+    if (C > 1 && crank == p.delay_cta && row == p.delay_row) spin_ns(p.delay_ns);
     __syncthreads();
-    if (warp == 0) {
-      float t = lane < nwarps ? s_warp[lane] : 0.f;
-      t = warp_sum(t);
-      const uint32_t b = it & 1u, par = (it >> 1) & 1u;
-      if (C > 1) {
-        // The butterfly leaves the same sum in every lane (at each step both
-        // lanes of a pair add the same two values, in either order, and fp32
-        // addition commutes), so lane r pushes it to CTA r
-        // and the C stores leave together: W = 8, M = 1, N = 8192 2.01 ->
-        // 1.96 us per call back to back; W = 16 2.16 -> 2.08 us.
+    float total;
+    if (C == 1) {
+      if (warp == 0) {
+        const float t = warp_sum(lane < nwarps ? s_warp[b][lane] : 0.f);
+        if (lane == 0) s_total = t;
+      }
+      __syncthreads();
+      total = s_total;
+    } else {
+      // s_warp[b], s_part[b] and s_xbar[b] are next written for row it + 2,
+      // after this CTA's first barrier of row it + 1, which every thread
+      // reaches only once it has read them for this row.
+      float t = warp_sum(lane < nwarps ? s_warp[b][lane] : 0.f);
+      const uint32_t par = (it >> 1) & 1u;
+      if (warp == 0) {
         if (lane == 0) mbar_arrive_expect_tx(&s_xbar[b], 4u * (uint32_t)C);
-        if (crank == p.delay_cta && row == p.delay_row) spin_ns(p.delay_ns);
         if (lane < C)
           st_async_f32(map_rank(&s_part[b][crank], (uint32_t)lane), t, map_rank(&s_xbar[b], (uint32_t)lane));
       }
-      if (lane == 0) {
-        if (C > 1) {
-          if (wait_cluster_phase(&s_xbar[b], par, p.wait_ns)) {
-            t = s_part[b][0];
-            for (int r = 1; r < C; r++) t += s_part[b][r];
-          } else {
-            atomicOr(p.err, 1u);
-            t = __int_as_float(0x7fc00000);  // NaN: this row's norm_out is not usable
-            // The missing partials may still come: wait (bounded again) until
-            // they have landed, so that none reaches this CTA's shared memory
-            // after it has exited and the barrier's phases stay in step for
-            // the next row.
-            if (!wait_cluster_phase(&s_xbar[b], par)) atomicOr(p.err, 2u);
-          }
-        }
-        s_total = t;
+      if (wait_cluster_phase(&s_xbar[b], par, p.wait_ns)) {
+        t = s_part[b][0];
+        for (int r = 1; r < C; r++) t += s_part[b][r];
+      } else {
+        atomicOr(p.err, 1u);
+        t = __int_as_float(0x7fc00000);  // NaN: this row's norm_out is not usable
+        // The missing partials may still come: wait (bounded again) until
+        // they have landed, so that none reaches this CTA's shared memory
+        // after it has exited and the barrier's phases stay in step for the
+        // next row.
+        if (!wait_cluster_phase(&s_xbar[b], par)) atomicOr(p.err, 2u);
       }
+      total = t;
     }
-    __syncthreads();
-    const float rms = rsqrtf(__fdiv_rn(s_total, p.cols) + p.eps);
+    const float rms = rsqrtf(__fdiv_rn(total, p.cols) + p.eps);
 
     // 4. normalise and scale
 #pragma unroll

@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
   constexpr int E = 8;
   constexpr int R = W > 0 ? W : kMaxRanks;
   const int n = W > 0 ? W : p.nranks;
-  __shared__ float s_warp[32];
-  __shared__ uint32_t s_miss_warp[32];
+  __shared__ float s_warp[2][32];        // warp partials, by row parity
+  __shared__ uint32_t s_miss_warp[2][32];  // warp masks, by row parity
   __shared__ __align__(8) uint2 s_part[2][8];  // the cluster's CTA (partial, mask) pairs, by row parity
   __shared__ __align__(8) uint64_t s_xbar[2];  // all C pairs of the row have landed, by row parity
   __shared__ float s_total;
@@ -176,62 +176,74 @@ __global__ void __launch_bounds__(max_threads<W, VPT>())
       }
     }
 
-    // row statistic and row "missing" mask: warp -> CTA -> cluster.  Split
-    // rows: each CTA pushes its (partial, mask) pair into every CTA of the
-    // cluster with st.async and combines the C pairs in rank order once they
-    // have landed, so every CTA of the row sees the same total and mask.
+    // row statistic and row "missing" mask: warp -> CTA -> cluster.  One
+    // CTA per row: warp 0 combines the warp pairs and broadcasts them through
+    // shared memory.  Split rows: every warp combines the warp pairs itself
+    // (same values, same order), lanes 0 .. C-1 of warp 0 push the CTA's
+    // (partial, mask) pair into every CTA of the cluster with st.async, and
+    // every thread combines the C pairs in rank order once they have landed,
+    // so every CTA of the row sees the same total and mask without a second
+    // CTA barrier (as in the fused row kernel).
     ss = warp_sum(ss);
     miss = __reduce_or_sync(0xFFFFFFFFu, miss);
+    const uint32_t b = it & 1u;
     if (lane == 0) {
-      s_warp[warp] = ss;
-      s_miss_warp[warp] = miss;
+      s_warp[b][warp] = ss;
+      s_miss_warp[b][warp] = miss;
     }
     if (!peers_ready) {
       cluster_wait();  // every peer's mbarriers are initialised
       peers_ready = true;
     }
     __syncthreads();
-    if (warp == 0) {
-      float t = lane < nwarps ? s_warp[lane] : 0.f;
-      uint32_t m = lane < nwarps ? s_miss_warp[lane] : 0u;
-      t = warp_sum(t);
-      m = __reduce_or_sync(0xFFFFFFFFu, m);
-      const uint32_t b = it & 1u;
-      if (C > 1) {
+    float total;
+    uint32_t row_miss;
+    if (C == 1) {
+      if (warp == 0) {
+        const float t = warp_sum(lane < nwarps ? s_warp[b][lane] : 0.f);
+        const uint32_t m = __reduce_or_sync(0xFFFFFFFFu, lane < nwarps ? s_miss_warp[b][lane] : 0u);
+        if (lane == 0) {
+          s_total = t;
+          s_miss = m;
+        }
+      }
+      __syncthreads();
+      total = s_total;
+      row_miss = s_miss;
+    } else {
+      // s_warp[b], s_miss_warp[b], s_part[b] and s_xbar[b] are next written
+      // for row it + 2, after this CTA's first barrier of row it + 1.
+      float t = warp_sum(lane < nwarps ? s_warp[b][lane] : 0.f);
+      uint32_t m = __reduce_or_sync(0xFFFFFFFFu, lane < nwarps ? s_miss_warp[b][lane] : 0u);
+      if (warp == 0) {
         // every lane holds the same (t, m); lane r pushes it to CTA r
         if (lane == 0) mbar_arrive_expect_tx(&s_xbar[b], 8u * (uint32_t)C);
         if (lane < C)
           st_async_v2_b32(map_rank(&s_part[b][crank], (uint32_t)lane), __float_as_uint(t), m,
                           map_rank(&s_xbar[b], (uint32_t)lane));
       }
-      if (lane == 0) {
-        if (C > 1) {
-          if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
-            t = __uint_as_float(s_part[b][0].x);
-            m = s_part[b][0].y;
-            for (int r = 1; r < C; r++) {
-              t += __uint_as_float(s_part[b][r].x);
-              m |= s_part[b][r].y;
-            }
-          } else {
-            atomicOr(p.err, 1u);
-            m = (1u << n) - 1u;  // the row's outputs are zeroed and every rank is logged for it
-            // Late partials may still land: wait for them (bounded again) so
-            // that none reaches this CTA's shared memory after it has exited.
-            if (!wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) atomicOr(p.err, 2u);
-          }
+      if (wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) {
+        t = __uint_as_float(s_part[b][0].x);
+        m = s_part[b][0].y;
+        for (int r = 1; r < C; r++) {
+          t += __uint_as_float(s_part[b][r].x);
+          m |= s_part[b][r].y;
         }
-        s_total = t;
-        s_miss = m;
+      } else {
+        atomicOr(p.err, 1u);
+        m = (1u << n) - 1u;  // the row's outputs are zeroed and every rank is logged for it
+        // Late partials may still land: wait for them (bounded again) so
+        // that none reaches this CTA's shared memory after it has exited.
+        if (!wait_cluster_phase(&s_xbar[b], (it >> 1) & 1u)) atomicOr(p.err, 2u);
       }
+      total = t;
+      row_miss = m;
     }
-    __syncthreads();
-    const uint32_t row_miss = s_miss;
     if (row_miss && crank == 0 && threadIdx.x == 0) {
       for (int r = 0; r < n; r++)
         if (row_miss >> r & 1u) log_stale(p.log, p.log_slot, (uint32_t)r, (uint32_t)row);
     }
-    const float rms = rsqrtf(__fdiv_rn(s_total, p.cols) + p.eps);
+    const float rms = rsqrtf(__fdiv_rn(total, p.cols) + p.eps);
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
       if (ok[k]) {
