@@ -166,10 +166,12 @@ __global__ void __launch_bounds__(max_threads<W, VPT>(), MINB)
     //    CTA barrier, and every CTA of the row sees the same total.  The
     //    butterfly leaves the same sum in every lane (at each step both lanes
     //    of a pair add the same two values, in either order, and fp32
-    //    addition commutes).  W = 8, M = 1, N = 8192: 2.01 -> 1.95 us per
-    //    call back to back; W = 16: 2.15 -> 2.08 us.  With one CTA per row
-    //    the second barrier stays: without it, many rows per CTA ran 1-2 %
-    //    slower.
+    //    addition commutes).  Back to back, W = 8, M = 1, N = 8192: 2.01 ->
+    //    1.96 us per call from pushing with C lanes instead of one, then
+    //    1.95 -> 1.84 us (another box) from dropping the second barrier;
+    //    W = 16: 2.08 -> 1.98 us.  With one CTA per row the second barrier
+    //    stays: every warp adding the partials itself there made many rows
+    //    per CTA 1-2 % slower.
     ss = warp_sum(ss);
     const uint32_t b = it & 1u;
     if (lane == 0) s_warp[b][warp] = ss;
