@@ -333,6 +333,32 @@ def test_fused_aliasing_and_no_ar(car, W, M, N, dtype, kernel):
     assert_norm_close(no, ref_no)
 
 
+@pytest.mark.parametrize("W,M,dtype,kernel", [
+    (16, 1, "bf16", "auto"),       # most ranks, one row split over a cluster
+    (3, 5, "fp32", "rows"),        # one CTA per row
+    (8, 200, "bf16", "auto"),      # more rows than SMs: the pipeline, with its ring cut to fit
+    (8, 200, "fp16", "rows"),
+    (2, 160, "bf16", "pipeline"),
+])
+def test_fused_at_the_longest_row(car, W, M, dtype, kernel):
+    """Rows of exactly CAR_MAX_ROW_BYTES: every output element against the oracle."""
+    N = car.CAR_MAX_ROW_BYTES // car_elem(dtype)
+    wl, xs, res, w = _fused_inputs(W, M, N, dtype, seed=2600 + W + M)
+    dx = [x.to(DEV) for x in xs]
+    dres, dw = res.to(DEV), w.to(DEV)
+    ro, no, ar = torch.empty_like(dres), torch.empty_like(dres), torch.empty_like(dres)
+    with car.Car(W, M, N, dtype) as c:
+        if kernel != "auto":
+            c.tune_fused(car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE)
+        c.reduce_residual_rmsnorm(dx, dres, dw, wl.eps, ro, no, ar)
+        c.sync()
+    torch.cuda.synchronize()
+    ref_ar, ref_ro, ref_no = oracle_fused(xs, res, w, wl.eps, M, N, dtype)
+    assert_bits_equal(ar, ref_ar, "ar")
+    assert_bits_equal(ro, ref_ro, "residual_out")
+    assert_norm_close(no, ref_no)
+
+
 def test_fused_rejects_rows_beyond_limit(car):
     N = car.CAR_MAX_ROW_BYTES // 2 + 8
     with car.Car(2, 1, N, "bf16") as c:
