@@ -335,10 +335,11 @@ car_status car_tune_fused(car_ctx* h, int kernel, int cluster, int threads, int 
  * then cleared).  Each wait is bounded to about one second: the pipelined
  * fused kernel's waits on its shared-memory barriers (it then stops and
  * leaves its remaining rows unwritten), and the waits of the fused row kernel
- * and the Lamport receive for the partials of a split row's other CTAs (the
- * row's norm_out is then NaN, or the Lamport row is reported stale for every
- * rank).  None of these waits runs out unless a CTA of the same launch has
- * stopped making progress. */
+ * and the Lamport receive for the partials of a split row's other CTAs (each
+ * thread waits for itself: the row's norm_out is then NaN in the columns of
+ * every thread whose wait ran out, or those columns of the Lamport row are
+ * zeroed and the row is reported stale for every rank).  None of these waits
+ * runs out unless a CTA of the same launch has stopped making progress. */
 car_status car_sync(car_ctx* h, void* stream);
 
 /* Test hook for the bounded wait of the fused row kernel (CAR_FUSED_ROWS
@@ -349,11 +350,12 @@ car_status car_sync(car_ctx* h, void* stream);
  * With cta in 0..7: the split row's partial exchange waits at most
  * wait_limit_ns (1000 .. 1e9) instead of about one second, and CTA `cta` of
  * the cluster that takes row `row` (0 .. M-1) reaches that row's exchange,
- * and so pushes its partial, delay_ns (at most CAR_TEST_MAX_DELAY_NS) late.  A peer whose wait runs out first
- * sets the handle's error flag (car_sync then returns CAR_ERR_TIMEOUT),
- * writes NaN for its columns of that row's norm_out, and then waits (bounded
- * by about one second) until the late partial has landed before it goes on,
- * so no partial reaches a CTA that has exited.  Every other output is
+ * and so pushes its partial, delay_ns (at most CAR_TEST_MAX_DELAY_NS) late.
+ * A thread of a peer whose wait runs out first sets the handle's error flag
+ * (car_sync then returns CAR_ERR_TIMEOUT), writes NaN for its columns of that
+ * row's norm_out, and then waits (bounded by about one second) until the late
+ * partial has landed before it goes on, so no partial reaches a CTA that has
+ * exited.  Every other output is
  * unaffected.  With cta = -1 (and the other arguments 0) the default returns.
  * Errors: CAR_ERR_ARG for values out of range, CAR_ERR_HANDLE. */
 #define CAR_TEST_MAX_DELAY_NS 100000000ull /* 100 ms */
