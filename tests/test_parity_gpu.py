@@ -268,7 +268,7 @@ def _degenerate_rows(W, M, N, seed):
     return xs, res, w
 
 
-@pytest.mark.parametrize("kernel,M", [("rows", 6), ("pipeline", 300)])
+@pytest.mark.parametrize("kernel,M", [("rows", 6), ("cluster", 6), ("pipeline", 300)])
 @pytest.mark.parametrize("eps", [1e-6, 0.0])
 def test_fused_degenerate_rows(car, kernel, M, eps):
     """ar and residual_out bit-exact, norm_out within tolerance, and NaN in
@@ -279,7 +279,10 @@ def test_fused_degenerate_rows(car, kernel, M, eps):
     dx = [x.to(DEV) for x in xs]
     ro, no, ar = (torch.empty(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(3))
     with car.Car(W, M, N, "bf16") as c:
-        c.tune_fused(car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE)
+        if kernel == "cluster":
+            c.tune_fused(car.CAR_FUSED_ROWS, 4, 32, 1)   # each row over 4 CTAs: the exchanged totals are inf / 0 too
+        else:
+            c.tune_fused(car.CAR_FUSED_ROWS if kernel == "rows" else car.CAR_FUSED_PIPELINE)
         c.reduce_residual_rmsnorm(dx, res.to(DEV), w.to(DEV), eps, ro, no, ar)
     torch.cuda.synchronize()
     assert_bits_equal(ar, ref_ar, "ar")
